@@ -1,0 +1,132 @@
+"""Seeded synthetic inputs for the MXFP4 latent-MoE layer.
+
+This module only draws random numbers in the shapes and distributions of the
+layer's workloads; it holds none of the layer's arithmetic. Both the CUDA path
+and the CPU oracle receive the same tensors from here.
+
+Workloads (the layer of "Kimi K3.1 Pro on AMD Instinct GPUs", "Kimi K3.1 Pro at
+a glance": 896 routed experts, top-16, intermediate 3,072 in a 3,584-wide
+latent; MXFP4 weights with one E8M0 scale per 32 values):
+
+  tiny                T=8,     d=256,  E=32,  k=4,  I=128
+  decode_t64          T=64,    d=3584, E=896, k=16, I=3072
+  decode_t512         T=512,   full dims
+  prefill_skewed_t8192  T=8192, full dims, logits + 2*ln(1/rank_e) for a random
+                      expert ranking (Zipf-like load)
+  prefill_outlier_t32768 T=32768, full dims, 1% of x rows scaled by 64
+
+Distributions: x ~ N(0,1) rounded to bf16; logits ~ N(0,1) fp32; weight codes
+are uniform random bytes (two uniform E2M1 codes each, all 16 codes including
+-0); weight scale codes uniform over the integers 118..122.
+
+Draw order from one torch.Generator seeded with `seed` on `device`: x, logits,
+expert ranking, outlier rows, w13 codes, w13 scales, w2 codes, w2 scales.
+A given (seed, device type) always gives the same tensors; the CPU and CUDA
+generators give different streams.
+"""
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    d: int
+    E: int
+    k: int
+    I: int
+    skew: bool = False          # add 2*ln(1/rank) per expert to the logits
+    outlier_frac: float = 0.0   # fraction of x rows scaled by outlier_scale
+    outlier_scale: float = 64.0
+
+
+WORKLOADS = [
+    Workload("tiny", T=8, d=256, E=32, k=4, I=128),
+    Workload("decode_t64", T=64, d=3584, E=896, k=16, I=3072),
+    Workload("decode_t512", T=512, d=3584, E=896, k=16, I=3072),
+    Workload("prefill_skewed_t8192", T=8192, d=3584, E=896, k=16, I=3072, skew=True),
+    Workload("prefill_outlier_t32768", T=32768, d=3584, E=896, k=16, I=3072,
+             outlier_frac=0.01),
+]
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def workload(name_or_index):
+    if isinstance(name_or_index, int):
+        return WORKLOADS[name_or_index]
+    return BY_NAME[name_or_index]
+
+
+def shape(name, T=None, d=None, E=None, k=None, I=None, **kw):
+    """A custom workload (test shapes)."""
+    return Workload(name, T=T, d=d, E=E, k=k, I=I, **kw)
+
+
+def _gen(seed, device):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def make_activations(wl: Workload, seed=0, device="cpu", g=None):
+    """x bf16 [T][d], logits fp32 [T][E] (draws 1-4 of the fixed order)."""
+    g = g if g is not None else _gen(seed, device)
+    T, d, E = wl.T, wl.d, wl.E
+    x = torch.randn(T, d, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    logits = torch.randn(T, E, generator=g, device=device, dtype=torch.float32)
+    if wl.skew:
+        order = torch.randperm(E, generator=g, device=device)
+        rank = torch.empty(E, dtype=torch.float32, device=device)
+        rank[order] = torch.arange(1, E + 1, dtype=torch.float32, device=device)
+        logits = logits + 2.0 * torch.log(1.0 / rank)[None, :]
+    if wl.outlier_frac > 0 and T > 0:
+        n_out = int(round(wl.outlier_frac * T))
+        rows = torch.randperm(T, generator=g, device=device)[:n_out]
+        x[rows] = (x[rows].float() * wl.outlier_scale).to(torch.bfloat16)
+    return x, logits
+
+
+def make_weights(wl: Workload, seed=0, device="cpu", g=None):
+    """Canonical MXFP4 weights (draws 5-8 of the fixed order).
+
+    w13 u8 [E][2I][d/2]: rows 0..I-1 gate (w1), rows I..2I-1 up (w3), two E2M1
+    codes per byte, the even element in the low nibble.
+    w13_s u8 [E][2I][d/32]: E8M0 scale codes, one per 32 consecutive inputs.
+    w2 u8 [E][d][I/2], w2_s u8 [E][d][I/32]: the down projection, same packing.
+    """
+    g = g if g is not None else _gen(seed, device)
+    E, d, I = wl.E, wl.d, wl.I
+    u8 = torch.uint8
+    w13 = torch.randint(0, 256, (E, 2 * I, d // 2), dtype=u8, generator=g, device=device)
+    w13_s = torch.randint(118, 123, (E, 2 * I, d // 32), dtype=u8, generator=g, device=device)
+    w2 = torch.randint(0, 256, (E, d, I // 2), dtype=u8, generator=g, device=device)
+    w2_s = torch.randint(118, 123, (E, d, I // 32), dtype=u8, generator=g, device=device)
+    return dict(w13=w13, w13_s=w13_s, w2=w2, w2_s=w2_s)
+
+
+def make_layer(wl: Workload, seed=0, device="cpu"):
+    """All inputs of one layer call in the fixed draw order."""
+    g = _gen(seed, device)
+    x, logits = make_activations(wl, g=g, device=device)
+    weights = make_weights(wl, g=g, device=device)
+    return dict(x=x, logits=logits, **weights)
+
+
+def random_e4m3_codes(shape_, seed=0, device="cpu", g=None):
+    """Uniform finite E4M3 codes (magnitude codes 0x00..0x7E, either sign)."""
+    g = g if g is not None else _gen(seed, device)
+    mag = torch.randint(0, 0x7F, shape_, dtype=torch.uint8, generator=g, device=device)
+    sign = torch.randint(0, 2, shape_, dtype=torch.uint8, generator=g, device=device) * 0x80
+    return mag | sign
+
+
+def random_scale_codes(shape_, lo=118, hi=122, seed=0, device="cpu", g=None):
+    g = g if g is not None else _gen(seed, device)
+    return torch.randint(lo, hi + 1, shape_, dtype=torch.uint8, generator=g, device=device)
+
+
+def bf16_bits(t):
+    """bf16 tensor -> its uint16 bit patterns as a numpy array (CPU)."""
+    return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view("uint16")

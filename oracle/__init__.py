@@ -1,0 +1,180 @@
+"""CPU oracle for the MXFP4 latent-MoE layer -- TEST INFRASTRUCTURE ONLY.
+
+Only tests/, the smoke check in __graft_entry__ and the CPU-baseline leg of
+bench.py may import this package. The CUDA product path never does.
+
+Thin ctypes wrapper over libmoe_oracle.so (built by oracle/build.py); numpy
+arrays in, numpy arrays out. Each function's arithmetic lives in
+moe_oracle.cpp, whose header cites the page sections it restates.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB, build_oracle
+
+_lib = None
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            build_oracle()
+        L = ctypes.CDLL(LIB)
+        sig = {
+            "orc_e2m1_value": (ctypes.c_double, [ctypes.c_uint8]),
+            "orc_e4m3_value": (ctypes.c_double, [ctypes.c_uint8]),
+            "orc_e8m0_value": (ctypes.c_double, [ctypes.c_uint8]),
+            "orc_e4m3_encode_rne_sat": (ctypes.c_uint8, [ctypes.c_double]),
+            "orc_mx_quant_block": (None, [_f32p, _u8p, _u8p]),
+            "orc_mx_quant_rows": (None, [_f32p, _i64, _i64, _u8p, _u8p]),
+            "orc_mx_quant_rows_bf16": (None, [_u16p, _i64, _i64, _u8p, _u8p]),
+            "orc_route_topk": (None, [_f32p, _i64, _i32, _i32, _i32p, _f32p]),
+            "orc_permute": (_i32, [_i32p, _i64, _i32, _i32, _i32, _i32p, _i32p, _i32p, _i32p, _i64]),
+            "orc_expert_stage1": (None, [_u8p, _u8p, _i32, _i32, _u8p, _u8p, _f64p]),
+            "orc_expert_stage2": (None, [_u8p, _u8p, _i32, _i32, _u8p, _u8p, _f64p]),
+            "orc_bf16_rne": (ctypes.c_uint16, [ctypes.c_double]),
+            "orc_moe_forward": (None, [_u16p, _f32p, _i64, _i32, _i32, _i32, _i32,
+                                       _u8p, _u8p, _u8p, _u8p, _u16p, _i32p, _f32p, _f64p, _i32]),
+            "orc_expert_bytes": (_i64, [_i32, _i32]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(a, ptype):
+    if a is None:
+        return ctypes.cast(None, ptype)
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ptype)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def e2m1_value(code):
+    return lib().orc_e2m1_value(int(code))
+
+
+def e4m3_value(code):
+    return lib().orc_e4m3_value(int(code))
+
+
+def e8m0_value(code):
+    return lib().orc_e8m0_value(int(code))
+
+
+def e4m3_encode(v):
+    return lib().orc_e4m3_encode_rne_sat(float(v))
+
+
+def bf16_rne(v):
+    return lib().orc_bf16_rne(float(v))
+
+
+def mx_quant_rows(v):
+    """fp32 [rows][K] -> (codes u8 [rows][K], scales u8 [rows][K/32])."""
+    v = _c(v, np.float32)
+    rows, K = v.shape
+    codes = np.empty((rows, K), np.uint8)
+    scales = np.empty((rows, K // 32), np.uint8)
+    lib().orc_mx_quant_rows(_p(v, _f32p), rows, K, _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales
+
+
+def mx_quant_rows_bf16(x_bits):
+    """bf16 bit patterns (uint16) [rows][K] -> (codes, scales)."""
+    x = _c(x_bits, np.uint16)
+    rows, K = x.shape
+    codes = np.empty((rows, K), np.uint8)
+    scales = np.empty((rows, K // 32), np.uint8)
+    lib().orc_mx_quant_rows_bf16(_p(x, _u16p), rows, K, _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales
+
+
+def route_topk(logits, k):
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float32)
+    lib().orc_route_topk(_p(lg, _f32p), T, E, k, _p(ids, _i32p), _p(w, _f32p))
+    return ids, w
+
+
+def permute(ids, E, pad_m, rows_capacity=None):
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    if rows_capacity is None:
+        rows_capacity = T * k + min(E, T * k) * (pad_m - 1)
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    slot_to_row = np.empty(T * k, np.int32)
+    row_to_slot = np.full(max(rows_capacity, 1), -7, np.int32)
+    rc = lib().orc_permute(_p(ids, _i32p), T, E, k, pad_m, _p(counts, _i32p), _p(offsets, _i32p),
+                           _p(slot_to_row, _i32p), _p(row_to_slot, _i32p), rows_capacity)
+    if rc != 0:
+        raise ValueError("oracle permute rejected its input")
+    return dict(counts=counts, offsets=offsets, slot_to_row=slot_to_row,
+                row_to_slot=row_to_slot[: int(offsets[E])])
+
+
+def expert_stage1(xq, xs, w13_e, w13s_e):
+    xq, xs = _c(xq, np.uint8), _c(xs, np.uint8)
+    w13_e, w13s_e = _c(w13_e, np.uint8), _c(w13s_e, np.uint8)
+    d = xq.shape[0]
+    I = w13_e.shape[0] // 2
+    h = np.empty(I, np.float64)
+    lib().orc_expert_stage1(_p(xq, _u8p), _p(xs, _u8p), d, I, _p(w13_e, _u8p),
+                            _p(w13s_e, _u8p), _p(h, _f64p))
+    return h
+
+
+def expert_stage2(hq, hs, w2_e, w2s_e):
+    hq, hs = _c(hq, np.uint8), _c(hs, np.uint8)
+    w2_e, w2s_e = _c(w2_e, np.uint8), _c(w2s_e, np.uint8)
+    I = hq.shape[0]
+    d = w2_e.shape[0]
+    y = np.empty(d, np.float64)
+    lib().orc_expert_stage2(_p(hq, _u8p), _p(hs, _u8p), I, d, _p(w2_e, _u8p),
+                            _p(w2s_e, _u8p), _p(y, _f64p))
+    return y
+
+
+def moe_forward(x_bits, logits, k, w13, w13s, w2, w2s, threads=0, want_y64=False):
+    """Whole layer for independent tokens. x_bits bf16 patterns [n][d].
+
+    Returns dict(y=bf16 bits [n][d], ids, w, y64 (or None)).
+    """
+    x = _c(x_bits, np.uint16)
+    lg = _c(logits, np.float32)
+    w13, w13s, w2, w2s = (_c(a, np.uint8) for a in (w13, w13s, w2, w2s))
+    n, d = x.shape
+    E = lg.shape[1]
+    I = w13.shape[1] // 2
+    y = np.empty((n, d), np.uint16)
+    ids = np.empty((n, max(k, 1)), np.int32)
+    w = np.empty((n, max(k, 1)), np.float32)
+    y64 = np.empty((n, d), np.float64) if want_y64 else None
+    lib().orc_moe_forward(_p(x, _u16p), _p(lg, _f32p), n, d, E, k, I, _p(w13, _u8p),
+                          _p(w13s, _u8p), _p(w2, _u8p), _p(w2s, _u8p), _p(y, _u16p),
+                          _p(ids, _i32p), _p(w, _f32p), _p(y64, _f64p), threads)
+    return dict(y=y, ids=ids[:, :k], w=w[:, :k], y64=y64)
+
+
+def expert_bytes(d, I):
+    return lib().orc_expert_bytes(d, I)

@@ -1,0 +1,65 @@
+"""A second, independent statement of the MX formats for the oracle pins.
+
+It decodes E2M1 from the OCP value list in tests/golden, E8M0 with numpy's
+ldexp and E4M3 with torch's float8_e4m3fn type, and quantises with numpy's
+frexp plus torch's RNE float8 cast (after clamping to +-448, since torch does
+not saturate). Nothing here comes from the oracle or from the CUDA library.
+"""
+import os
+
+import numpy as np
+import torch
+
+_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "e2m1_values.txt")
+
+
+def e2m1_table():
+    vals = []
+    with open(_GOLDEN) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                vals.extend(float(t) for t in line.split())
+    return np.array(vals, np.float64)
+
+
+def e4m3_decode(codes):
+    c = torch.from_numpy(np.ascontiguousarray(codes, np.uint8))
+    return c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def e8m0_decode(codes):
+    return np.ldexp(1.0, np.asarray(codes, np.int64) - 127)
+
+
+def decode_mxfp4(packed, scales):
+    """packed u8 [..., R, K/2], scales u8 [..., R, K/32] -> fp64 [..., R, K]."""
+    packed = np.asarray(packed, np.uint8)
+    lo, hi = packed & 0xF, packed >> 4
+    codes = np.stack([lo, hi], axis=-1).reshape(*packed.shape[:-1], packed.shape[-1] * 2)
+    vals = e2m1_table()[codes]
+    sc = np.repeat(e8m0_decode(scales), 32, axis=-1)
+    return vals * sc
+
+
+def decode_mxfp8(codes, scales):
+    return e4m3_decode(codes) * np.repeat(e8m0_decode(scales), 32, axis=-1)
+
+
+def quant_mxfp8(v):
+    """fp32 [rows][K] -> (codes, scales) by the OCP MX rule with saturation."""
+    v = np.asarray(v, np.float32)
+    rows, K = v.shape
+    b = v.astype(np.float64).reshape(rows, K // 32, 32)
+    amax = np.abs(b).max(axis=2)
+    _, ex = np.frexp(amax)
+    sc = np.clip(ex - 1 - 8 + 127, 0, 254)
+    sc[amax == 0] = 0
+    q = np.clip(b / np.ldexp(1.0, sc - 127)[:, :, None], -448.0, 448.0)
+    codes = torch.from_numpy(np.ascontiguousarray(q)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return codes.reshape(rows, K), sc.astype(np.uint8)
+
+
+def bf16_bits_to_f64(bits):
+    b = np.asarray(bits, np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
