@@ -1,0 +1,229 @@
+/*
+ * moe.h -- C-ABI of libmoe.so, the GB300 (sm_103a) MXFP4 latent-MoE layer.
+ *
+ * The layer (sources are page titles and sections):
+ *   "Kimi K3.1 Pro on AMD Instinct GPUs", "Kimi K3.1 Pro at a glance":
+ *     896 routed experts, 16 active per token, sigmoid routing, expert
+ *     intermediate 3,072 in a 3,584-wide latent, SiTU-GLU activation,
+ *     routed experts in MXFP4 with one E8M0 scale per 32 values.
+ *   same page, "Serving with ATOM / What we optimized", "The MXFP4 latent MoE
+ *     on FlyDSL": a grouped-MoE kernel, MXFP4 weights, FP8 second stage.
+ *   "Day 0 Kimi-K3 Inference Deployment with ATOM on AMD Instinct MI355X
+ *     GPUs", "Model Architecture" table and "HBM Usage Under TP8" (w1/w2/w3).
+ *
+ * Readings where the pages are silent: SwiGLU stands in for the undefined
+ * SiTU-GLU (h = silu(gate) * up); w1 = gate, w3 = up, w2 = down; scale blocks
+ * of 32 run along the reduction dimension; activations of both stages are
+ * MXFP8 (E4M3 + one E8M0 per 32, OCP MX rule, round-to-nearest-even with
+ * saturation to +-448); selection on the logits with ties to the lower id,
+ * weights = sigmoid(l_j) / sum of the k selected sigmoids.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller, unless stated. The
+ *    library never allocates or frees device memory and never synchronises,
+ *    except moe_check_device_status.
+ *  - Work is enqueued on `stream` in order; the host returns without waiting.
+ *  - Arguments are validated on the host before any launch. A failed check
+ *    returns a non-zero moe_status and enqueues nothing.
+ *  - Launch failures return MOE_ERR_CUDA. Problems found on the device (a
+ *    bounded wait that ran out, an expert id out of range) are recorded in the
+ *    4-byte status word at the start of the workspace `ws`; read it with
+ *    moe_check_device_status. The GPU never traps.
+ *  - bf16 tensors are passed as uint16_t bit patterns.
+ *  - All work runs on the CUDA device current in the calling thread.
+ *  - Thread-safe as long as concurrent calls use distinct workspaces.
+ *
+ * Shapes (checked; anything else is MOE_ERR_UNSUPPORTED):
+ *   1 <= E <= 1024, 0 <= k <= min(E, 32), T >= 0, T*k < 2^31,
+ *   d % 128 == 0 and I % 128 == 0 (both >= 128),
+ *   pad_m == 128 for the grouped GEMMs and moe_forward; moe_permute takes any
+ *   power of two 1..1024.
+ *
+ * Data layouts:
+ *   x, y        bf16 [T][d] row-major.
+ *   logits      fp32 [T][E].
+ *   topk_ids    int32 [T][k], topk_w fp32 [T][k]; slot s = t*k + j.
+ *   Weights     w13 u8 [E][2I][d/2]: rows 0..I-1 gate (w1), I..2I-1 up (w3);
+ *               w2 u8 [E][d][I/2]; two E2M1 codes per byte, even element in
+ *               the low nibble. Canonical scales are u8 [rows][K/32] (one
+ *               E8M0 code per 32 consecutive inputs); the GEMMs take them in
+ *               the TILED layout below, made once by moe_prepack_scales.
+ *   Activations xq u8 [rows][d] and hq u8 [rows][I] E4M3 codes; their scales
+ *               in the TILED layout.
+ *   TILED scale layout of an operand with R rows and K inputs per row (R
+ *   rounded up to 128, K % 128 == 0): the scale of row r, 32-block b is byte
+ *     ((r/128)*(K/128) + b/4)*512 + (r%32)*16 + ((r/32)%4)*4 + b%4,
+ *   i.e. one 512-byte atom per 128 rows x 128 inputs, in the order the
+ *   tensor-core scale-factor copy reads it.
+ *   Grouped rows: rows [offsets[e], offsets[e+1]) belong to expert e, the
+ *   first counts[e] of them hold its tokens in ascending token order, the rest
+ *   are padding (row_to_slot == -1, contents unspecified, never read back).
+ */
+#ifndef MXFP4_LATENT_MOE_H
+#define MXFP4_LATENT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARGUMENT = 1,    /* null pointer, negative size, bad alignment */
+  MOE_ERR_UNSUPPORTED = 2,         /* shape outside the supported set */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes or rows_capacity below what the call needs */
+  MOE_ERR_CUDA = 4,                /* a CUDA runtime/driver call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5,      /* device status: a bounded wait ran out */
+  MOE_ERR_DEVICE_BAD_INPUT = 6     /* device status: expert id out of range or repeated */
+} moe_status;
+
+typedef struct {
+  int32_t T; /* tokens */
+  int32_t d; /* latent width (3584) */
+  int32_t E; /* routed experts (896) */
+  int32_t k; /* experts per token (16) */
+  int32_t I; /* expert intermediate width (3072) */
+} moe_dims;
+
+typedef struct {
+  const uint8_t* w13;    /* [E][2I][d/2] packed E2M1 */
+  const uint8_t* w13_sf; /* TILED scales of w13 viewed as [E*2I][d] (moe_prepack_scales) */
+  const uint8_t* w2;     /* [E][d][I/2] packed E2M1 */
+  const uint8_t* w2_sf;  /* TILED scales of w2 viewed as [E*d][I] */
+} moe_weights;
+
+/* Bytes of the device status word region at the start of every workspace. */
+#define MOE_STATUS_BYTES 256
+
+/* Short English text of a status code. Never NULL; static storage. */
+const char* moe_status_string(moe_status s);
+
+/* Version of this ABI (incremented on incompatible change). */
+int32_t moe_abi_version(void);
+
+/* Bytes of a TILED scale array for `rows` rows of K inputs (rows rounded up
+ * to a multiple of 128). Returns 0 for unsupported K. */
+size_t moe_tiled_scale_bytes(int64_t rows, int32_t K);
+
+/* Rows a grouped activation buffer needs for T tokens, k experts each, E
+ * experts and padding pad_m: T*k + min(E, T*k)*(pad_m-1), rounded up to 128. */
+int64_t moe_rows_capacity(int32_t T, int32_t E, int32_t k, int32_t pad_m);
+
+/* Canonical scales [rows][K/32] -> TILED layout (moe_tiled_scale_bytes bytes).
+ * One-time weight preparation; the bytes are permuted, not changed. Rows past
+ * `rows` in the last 128-row atom are written as 0. src and dst must not
+ * overlap; dst 16-byte aligned. */
+moe_status moe_prepack_scales(const uint8_t* src, int64_t rows, int32_t K, uint8_t* dst,
+                              cudaStream_t stream);
+
+/* Sigmoid top-k routing ("Kimi K3.1 Pro at a glance", Experts row: "896
+ * routed (top-16, sigmoid routing)").
+ * For each token t: the k largest logits[t][:], ordered by logit descending
+ * and expert id ascending on ties (IEEE compare, -0 == +0);
+ * topk_w[t][j] = sigmoid(l_j) / sum_j' sigmoid(l_j') in fp32.
+ * logits fp32 [T][E] (finite); outputs int32 [T][k] and fp32 [T][k]. */
+moe_status moe_route_topk(const float* logits, int32_t T, int32_t E, int32_t k,
+                          int32_t* topk_ids, float* topk_w, cudaStream_t stream);
+
+/* Workspace bytes moe_permute needs (status word + per-chunk histograms). */
+size_t moe_permute_workspace_size(int32_t T, int32_t E);
+
+/* Expert grouping for the grouped-MoE kernel ("The MXFP4 latent MoE on
+ * FlyDSL"): histogram, exclusive scan of padded counts, stable scatter.
+ * counts [E]; offsets [E+1] with offsets[e+1] = offsets[e] +
+ * ceil(counts[e]/pad_m)*pad_m; slot_to_row [T*k]; row_to_slot [rows_capacity]
+ * (slot of each grouped row, -1 on padding rows, untouched past offsets[E]).
+ * Within an expert, rows follow ascending token order: the result is unique
+ * and does not depend on scheduling. rows_capacity must be at least
+ * moe_rows_capacity(T, E, k, pad_m) (checked on the host). An id out of range
+ * or repeated within a token sets MOE_ERR_DEVICE_BAD_INPUT in the status word
+ * and leaves the outputs unspecified. */
+moe_status moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k, int32_t pad_m,
+                       int32_t* counts, int32_t* offsets, int32_t* slot_to_row,
+                       int32_t* row_to_slot, int64_t rows_capacity, void* ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/* MXFP8 quantisation of the stage-1 activations (OCP MX rule, E4M3 + E8M0
+ * per 32 consecutive values of a row): per block, scale code
+ * c = clamp(floor(log2(amax)) - 8 + 127, 0, 254) (0 for an all-zero block),
+ * element codes = E4M3 round-to-nearest-even of x * 2^(127-c) saturated to
+ * +-448, the sign kept on zero results.
+ * x bf16 [T][d]. With slot_to_row == NULL the output rows are the tokens
+ * (row t); otherwise token t is written to every row slot_to_row[t*k + j],
+ * j < k. codes u8 [rows_capacity][d]; scales TILED for (rows_capacity, d).
+ * rows_capacity % 128 == 0. */
+moe_status moe_quant_mxfp8(const uint16_t* x, int32_t T, int32_t d, const int32_t* slot_to_row,
+                           int32_t k, uint8_t* codes, uint8_t* scales, int64_t rows_capacity,
+                           cudaStream_t stream);
+
+/* Stage 1 grouped GEMM on tcgen05 block-scaled tensor cores
+ * (kind::mxf8f6f4, MXFP8 activations x MXFP4 weights, fp32 accumulation)
+ * with the GLU and the FP8 second-stage quantisation fused in the epilogue
+ * ("The MXFP4 latent MoE on FlyDSL"; expert shapes from the Experts row).
+ * For each expert e and each grouped row r in [offsets[e], offsets[e+1]):
+ *   g = X[r] . W1[e]^T, u = X[r] . W3[e]^T  (dequantised operands, fp32 sums)
+ *   h = silu(g) * u (fp32), then MXFP8 as in moe_quant_mxfp8
+ *   -> hq [r][I] codes and hs TILED scales for (rows_capacity, I).
+ * offsets int32 [E+1] is read on the device; offsets[E] <= rows_capacity and
+ * offsets[e] % pad_m == 0 are the caller's (moe_permute's) guarantee.
+ * ws: at least MOE_STATUS_BYTES; the status word records timeouts.
+ * xq, hq 16-byte aligned; w13 32-byte aligned; scale arrays 16-byte aligned. */
+moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets,
+                                    int32_t E, int32_t d, int32_t I, int32_t pad_m,
+                                    const uint8_t* w13, const uint8_t* w13_sf, uint8_t* hq,
+                                    uint8_t* hs, int64_t rows_capacity, void* ws,
+                                    size_t ws_bytes, cudaStream_t stream);
+
+/* Stage 2 grouped GEMM (the down projection w2, 3,072 -> 3,584 in the pages'
+ * layer): Yp[r] = H[r] . W2[e]^T with MXFP8 H and MXFP4 W2 on tcgen05
+ * block-scaled tensor cores, fp32 accumulation, rounded to bf16.
+ * yp bf16 [rows_capacity][d], 16-byte aligned. Other arguments as above. */
+moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32_t* offsets,
+                               int32_t E, int32_t I, int32_t d, int32_t pad_m,
+                               const uint8_t* w2, const uint8_t* w2_sf, uint16_t* yp,
+                               int64_t rows_capacity, void* ws, size_t ws_bytes,
+                               cudaStream_t stream);
+
+/* Routing-weighted combine: y[t] = bf16_rne(sum_{j=0..k-1} topk_w[t][j] *
+ * Yp[slot_to_row[t*k+j]]) with fp32 accumulation in j order. k == 0 gives
+ * y = 0. yp, y 16-byte aligned. */
+moe_status moe_unpermute_combine(const uint16_t* yp, const int32_t* slot_to_row,
+                                 const float* topk_w, int32_t T, int32_t k, int32_t d,
+                                 uint16_t* y, cudaStream_t stream);
+
+/* Workspace bytes moe_forward needs for these dims and pad_m. */
+moe_status moe_workspace_size(const moe_dims* dims, int32_t pad_m, size_t* bytes);
+
+/* The whole layer: route -> permute -> quantise -> stage-1 GEMM + GLU +
+ * requant -> stage-2 GEMM -> combine, all on `stream` with no host
+ * synchronisation. Clears the status word at its start.
+ * x bf16 [T][d], logits fp32 [T][E], weights as in moe_weights, y bf16 [T][d].
+ * topk_ids_out / topk_w_out may be NULL; if given they receive the routing.
+ * ws: moe_workspace_size bytes, 256-byte aligned. */
+moe_status moe_forward(const moe_dims* dims, int32_t pad_m, const uint16_t* x,
+                       const float* logits, const moe_weights* weights, uint16_t* y,
+                       int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/* Synchronises `stream`, then returns the status recorded in the workspace's
+ * status word (MOE_OK if none). */
+moe_status moe_check_device_status(const void* ws, cudaStream_t stream);
+
+/* Enqueues a reset of the status word to MOE_OK. */
+moe_status moe_clear_device_status(void* ws, cudaStream_t stream);
+
+/* Self-test of the bounded device wait used by the GEMM pipelines: one CTA
+ * waits on a shared-memory barrier that nothing signals, gives up after
+ * `limit_us` microseconds and records MOE_ERR_DEVICE_TIMEOUT in the status
+ * word. Never hangs or traps; the context stays usable. */
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us,
+                                     cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

@@ -1,0 +1,197 @@
+"""ctypes binding of libmoe.so (include/moe.h): the same entry-point names,
+torch tensors in, argument marshalling only. Every step of the layer runs in
+the library's CUDA kernels; nothing here computes any part of it.
+
+The library is loaded on first use. If it has not been built, or no CUDA
+device is present, calls raise instead of falling back to anything else.
+"""
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+
+STATUS_BYTES = 256
+OK, INVALID_ARGUMENT, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA, DEVICE_TIMEOUT, DEVICE_BAD_INPUT = range(7)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, code, text):
+        super().__init__("%s failed: status %d (%s)" % (fn, code, text))
+        self.code = code
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+
+
+class _Dims(ctypes.Structure):
+    _fields_ = [("T", _i32), ("d", _i32), ("E", _i32), ("k", _i32), ("I", _i32)]
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [("w13", _vp), ("w13_sf", _vp), ("w2", _vp), ("w2_sf", _vp)]
+
+
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [_i32]),
+    "moe_abi_version": (_i32, []),
+    "moe_tiled_scale_bytes": (_sz, [_i64, _i32]),
+    "moe_rows_capacity": (_i64, [_i32, _i32, _i32, _i32]),
+    "moe_prepack_scales": (_i32, [_vp, _i64, _i32, _vp, _vp]),
+    "moe_route_topk": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "moe_permute_workspace_size": (_sz, [_i32, _i32]),
+    "moe_permute": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
+    "moe_quant_mxfp8": (_i32, [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _i64, _vp]),
+    "moe_grouped_gemm_w13_glu": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
+                                        _i64, _vp, _sz, _vp]),
+    "moe_grouped_gemm_w2": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i64, _vp,
+                                   _sz, _vp]),
+    "moe_unpermute_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
+    "moe_workspace_size": (_i32, [ctypes.POINTER(_Dims), _i32, ctypes.POINTER(_sz)]),
+    "moe_forward": (_i32, [ctypes.POINTER(_Dims), _i32, _vp, _vp, ctypes.POINTER(_Weights), _vp,
+                           _vp, _vp, _vp, _sz, _vp]),
+    "moe_check_device_status": (_i32, [_vp, _vp]),
+    "moe_clear_device_status": (_i32, [_vp, _vp]),
+    "moe_selftest_wait_timeout": (_i32, [_vp, _sz, ctypes.c_uint32, _vp]),
+}
+
+EXPORTED = tuple(_SIGS)
+
+
+def lib():
+    """The loaded library (raises if it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libmoe.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(code):
+    return lib().moe_status_string(int(code)).decode()
+
+
+def _check(name, code):
+    if code != OK:
+        raise MoeError(name, code, status_string(code))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _call(name, *args):
+    _check(name, getattr(lib(), name)(*args))
+
+
+# ---------------------------------------------------------------- sizes
+
+def moe_abi_version():
+    return lib().moe_abi_version()
+
+
+def moe_tiled_scale_bytes(rows, K):
+    return lib().moe_tiled_scale_bytes(rows, K)
+
+
+def moe_rows_capacity(T, E, k, pad_m):
+    return lib().moe_rows_capacity(T, E, k, pad_m)
+
+
+def moe_permute_workspace_size(T, E):
+    return lib().moe_permute_workspace_size(T, E)
+
+
+def moe_workspace_size(T, d, E, k, I, pad_m=128):
+    out = _sz(0)
+    _check("moe_workspace_size", lib().moe_workspace_size(ctypes.byref(_Dims(T, d, E, k, I)), pad_m,
+                                                          ctypes.byref(out)))
+    return out.value
+
+
+# ---------------------------------------------------------------- entry points
+
+def moe_prepack_scales(src, rows, K, dst, stream=None):
+    _call("moe_prepack_scales", _ptr(src), rows, K, _ptr(dst), _stream(stream))
+
+
+def moe_route_topk(logits, T, E, k, topk_ids, topk_w, stream=None):
+    _call("moe_route_topk", _ptr(logits), T, E, k, _ptr(topk_ids), _ptr(topk_w), _stream(stream))
+
+
+def moe_permute(topk_ids, T, E, k, pad_m, counts, offsets, slot_to_row, row_to_slot,
+                rows_capacity, ws, stream=None):
+    _call("moe_permute", _ptr(topk_ids), T, E, k, pad_m, _ptr(counts), _ptr(offsets),
+          _ptr(slot_to_row), _ptr(row_to_slot), rows_capacity, _ptr(ws), ws.numel() * ws.element_size(),
+          _stream(stream))
+
+
+def moe_quant_mxfp8(x, T, d, slot_to_row, k, codes, scales, rows_capacity, stream=None):
+    _call("moe_quant_mxfp8", _ptr(x), T, d, _ptr(slot_to_row), k, _ptr(codes), _ptr(scales),
+          rows_capacity, _stream(stream))
+
+
+def moe_grouped_gemm_w13_glu(xq, xs, offsets, E, d, I, pad_m, w13, w13_sf, hq, hs, rows_capacity,
+                             ws, stream=None):
+    _call("moe_grouped_gemm_w13_glu", _ptr(xq), _ptr(xs), _ptr(offsets), E, d, I, pad_m, _ptr(w13),
+          _ptr(w13_sf), _ptr(hq), _ptr(hs), rows_capacity, _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def moe_grouped_gemm_w2(hq, hs, offsets, E, I, d, pad_m, w2, w2_sf, yp, rows_capacity, ws,
+                        stream=None):
+    _call("moe_grouped_gemm_w2", _ptr(hq), _ptr(hs), _ptr(offsets), E, I, d, pad_m, _ptr(w2),
+          _ptr(w2_sf), _ptr(yp), rows_capacity, _ptr(ws), ws.numel() * ws.element_size(),
+          _stream(stream))
+
+
+def moe_unpermute_combine(yp, slot_to_row, topk_w, T, k, d, y, stream=None):
+    _call("moe_unpermute_combine", _ptr(yp), _ptr(slot_to_row), _ptr(topk_w), T, k, d, _ptr(y),
+          _stream(stream))
+
+
+def moe_forward(T, d, E, k, I, pad_m, x, logits, w13, w13_sf, w2, w2_sf, y, ws,
+                topk_ids_out=None, topk_w_out=None, stream=None):
+    W = _Weights(_ptr(w13), _ptr(w13_sf), _ptr(w2), _ptr(w2_sf))
+    _call("moe_forward", ctypes.byref(_Dims(T, d, E, k, I)), pad_m, _ptr(x), _ptr(logits),
+          ctypes.byref(W), _ptr(y), _ptr(topk_ids_out), _ptr(topk_w_out), _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def moe_check_device_status(ws, stream=None):
+    """Synchronises the stream; returns the device status code (0 = ok)."""
+    return lib().moe_check_device_status(_ptr(ws), _stream(stream))
+
+
+def moe_clear_device_status(ws, stream=None):
+    _call("moe_clear_device_status", _ptr(ws), _stream(stream))
+
+
+def moe_selftest_wait_timeout(ws, limit_us, stream=None):
+    _call("moe_selftest_wait_timeout", _ptr(ws), ws.numel() * ws.element_size(), limit_us,
+          _stream(stream))

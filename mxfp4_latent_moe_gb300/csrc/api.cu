@@ -1,0 +1,334 @@
+// C-ABI of libmoe.so: argument validation, workspace layout, launches.
+// The contract of every entry point is stated in include/moe.h.
+#include <climits>
+
+#include "internal.h"
+
+namespace {
+
+using moe::tiled_sf_offset;
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kGemmPad = 128;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status check_routing_shape(int32_t T, int32_t E, int32_t k) {
+  if (T < 0 || E < 0 || k < 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (E < 1 || E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
+  if (int64_t(T) * k >= int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_width(int32_t w) {
+  if (w < 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (w < 128 || w % 128 != 0 || w > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool pow2_in(int32_t v, int32_t lo, int32_t hi) {
+  return v >= lo && v <= hi && (v & (v - 1)) == 0;
+}
+
+int64_t rows_capacity_of(int32_t T, int32_t E, int32_t k, int32_t pad_m) {
+  const int64_t slots = int64_t(T) * k;
+  const int64_t rows = slots + (slots < E ? slots : int64_t(E)) * (pad_m - 1);
+  return (rows + 127) / 128 * 128;
+}
+
+size_t tiled_bytes(int64_t rows, int32_t K) {
+  const int64_t rp = (rows + 127) / 128 * 128;
+  return size_t(rp) * size_t(K / 32);
+}
+
+struct ForwardLayout {
+  size_t status, hist, ids, w, counts, offsets, s2r, r2s, xq, xs, hq, hs, yp, total;
+  int64_t rows_cap;
+};
+
+ForwardLayout forward_layout(const moe_dims& D, int32_t pad_m) {
+  ForwardLayout L{};
+  const size_t slots = size_t(D.T) * size_t(D.k);
+  L.rows_cap = rows_capacity_of(D.T, D.E, D.k, pad_m);
+  const size_t rc = size_t(L.rows_cap);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += round_up(bytes, 256);
+    return o;
+  };
+  L.status = take(MOE_STATUS_BYTES);
+  L.hist = take(moe::permute_scratch_bytes(D.T, D.E));
+  L.ids = take(slots * 4);
+  L.w = take(slots * 4);
+  L.counts = take(size_t(D.E) * 4);
+  L.offsets = take(size_t(D.E + 1) * 4);
+  L.s2r = take(slots * 4);
+  L.r2s = take(rc * 4);
+  L.xq = take(rc * size_t(D.d));
+  L.xs = take(tiled_bytes(L.rows_cap, D.d));
+  L.hq = take(rc * size_t(D.I));
+  L.hs = take(tiled_bytes(L.rows_cap, D.I));
+  L.yp = take(rc * size_t(D.d) * 2);
+  L.total = off;
+  return L;
+}
+
+moe_status check_dims(const moe_dims* D) {
+  if (!D) return MOE_ERR_INVALID_ARGUMENT;
+  moe_status s = check_routing_shape(D->T, D->E, D->k);
+  if (s != MOE_OK) return s;
+  if ((s = check_width(D->d)) != MOE_OK) return s;
+  return check_width(D->I);
+}
+
+moe_status check_gemm_args(int32_t E, int32_t K, int32_t N, int32_t pad_m, int64_t rows_capacity,
+                           const void* a, const void* a_sf, const int32_t* offsets,
+                           const void* b, const void* b_sf, const void* out, const void* out_sf,
+                           bool need_out_sf, const void* ws, size_t ws_bytes) {
+  if (!a || !a_sf || !offsets || !b || !b_sf || !out || !ws || (need_out_sf && !out_sf))
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (E < 0 || rows_capacity < 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (E < 1 || E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  moe_status s;
+  if ((s = check_width(K)) != MOE_OK) return s;
+  if ((s = check_width(N)) != MOE_OK) return s;
+  if (pad_m != kGemmPad) return MOE_ERR_UNSUPPORTED;
+  if (rows_capacity % 128 != 0 || rows_capacity >= int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(a, 16) || !aligned(a_sf, 16) || !aligned(b, 32) || !aligned(b_sf, 16) ||
+      !aligned(out, 16) || (need_out_sf && !aligned(out_sf, 4)) || !aligned(offsets, 4) ||
+      !aligned(ws, 4))
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < MOE_STATUS_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+template <class T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace or row capacity too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device: a bounded wait ran out";
+    case MOE_ERR_DEVICE_BAD_INPUT: return "device: bad expert ids or offsets";
+  }
+  return "unknown status";
+}
+
+int32_t moe_abi_version(void) { return 1; }
+
+size_t moe_tiled_scale_bytes(int64_t rows, int32_t K) {
+  if (rows < 0 || check_width(K) != MOE_OK) return 0;
+  return tiled_bytes(rows, K);
+}
+
+int64_t moe_rows_capacity(int32_t T, int32_t E, int32_t k, int32_t pad_m) {
+  if (check_routing_shape(T, E, k) != MOE_OK || !pow2_in(pad_m, 1, 1024)) return -1;
+  return rows_capacity_of(T, E, k, pad_m);
+}
+
+moe_status moe_prepack_scales(const uint8_t* src, int64_t rows, int32_t K, uint8_t* dst,
+                              cudaStream_t stream) {
+  if (rows < 0) return MOE_ERR_INVALID_ARGUMENT;
+  moe_status s = check_width(K);
+  if (s != MOE_OK) return s;
+  if (rows == 0) return MOE_OK;
+  if (!src || !dst || !aligned(dst, 16)) return MOE_ERR_INVALID_ARGUMENT;
+  return from_cuda(moe::launch_prepack_scales(src, rows, K, dst, stream));
+}
+
+moe_status moe_route_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_ids,
+                          float* topk_w, cudaStream_t stream) {
+  moe_status s = check_routing_shape(T, E, k);
+  if (s != MOE_OK) return s;
+  if (T == 0 || k == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+    return MOE_ERR_INVALID_ARGUMENT;
+  return from_cuda(moe::launch_route_topk(logits, T, E, k, topk_ids, topk_w, stream));
+}
+
+size_t moe_permute_workspace_size(int32_t T, int32_t E) {
+  if (T < 0 || E < 1 || E > kMaxE) return 0;
+  return MOE_STATUS_BYTES + round_up(moe::permute_scratch_bytes(T, E), 256);
+}
+
+moe_status moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k, int32_t pad_m,
+                       int32_t* counts, int32_t* offsets, int32_t* slot_to_row,
+                       int32_t* row_to_slot, int64_t rows_capacity, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  moe_status s = check_routing_shape(T, E, k);
+  if (s != MOE_OK) return s;
+  if (!pow2_in(pad_m, 1, 1024)) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !ws || rows_capacity < 0) return MOE_ERR_INVALID_ARGUMENT;
+  const bool any = T > 0 && k > 0;
+  if (any && (!topk_ids || !slot_to_row || !row_to_slot)) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(counts, 4) || !aligned(offsets, 4) || !aligned(ws, 4) ||
+      (any && (!aligned(topk_ids, 4) || !aligned(slot_to_row, 4) || !aligned(row_to_slot, 4))))
+    return MOE_ERR_INVALID_ARGUMENT;
+  const int64_t slots = int64_t(T) * k;
+  if (rows_capacity < slots + (slots < E ? slots : int64_t(E)) * (pad_m - 1))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < moe_permute_workspace_size(T, E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(moe::launch_permute(topk_ids, T, E, k, pad_m, counts, offsets, slot_to_row,
+                                       row_to_slot, at<int>(ws, MOE_STATUS_BYTES),
+                                       static_cast<int*>(ws), stream));
+}
+
+moe_status moe_quant_mxfp8(const uint16_t* x, int32_t T, int32_t d, const int32_t* slot_to_row,
+                           int32_t k, uint8_t* codes, uint8_t* scales, int64_t rows_capacity,
+                           cudaStream_t stream) {
+  if (T < 0 || k < 0 || rows_capacity < 0) return MOE_ERR_INVALID_ARGUMENT;
+  moe_status s = check_width(d);
+  if (s != MOE_OK) return s;
+  if (k > kMaxK || int64_t(T) * (k > 0 ? k : 1) >= int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  if (rows_capacity % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0 || (slot_to_row && k == 0)) return MOE_OK;
+  if (!x || !codes || !scales) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || !aligned(codes, 8) || !aligned(scales, 4) ||
+      (slot_to_row && !aligned(slot_to_row, 4)))
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (!slot_to_row && rows_capacity < T) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(moe::launch_quant_mxfp8(x, T, d, slot_to_row, k, codes, scales, stream));
+}
+
+moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets,
+                                    int32_t E, int32_t d, int32_t I, int32_t pad_m,
+                                    const uint8_t* w13, const uint8_t* w13_sf, uint8_t* hq,
+                                    uint8_t* hs, int64_t rows_capacity, void* ws,
+                                    size_t ws_bytes, cudaStream_t stream) {
+  moe_status s = check_gemm_args(E, d, I, pad_m, rows_capacity, xq, xs, offsets, w13, w13_sf, hq,
+                                 hs, true, ws, ws_bytes);
+  if (s != MOE_OK) return s;
+  if (rows_capacity == 0) return MOE_OK;
+  return from_cuda(moe::launch_gemm_w13_glu(xq, xs, offsets, E, d, I, w13, w13_sf, hq, hs,
+                                            rows_capacity, static_cast<int*>(ws), stream));
+}
+
+moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32_t* offsets,
+                               int32_t E, int32_t I, int32_t d, int32_t pad_m,
+                               const uint8_t* w2, const uint8_t* w2_sf, uint16_t* yp,
+                               int64_t rows_capacity, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  moe_status s = check_gemm_args(E, I, d, pad_m, rows_capacity, hq, hs, offsets, w2, w2_sf, yp,
+                                 nullptr, false, ws, ws_bytes);
+  if (s != MOE_OK) return s;
+  if (rows_capacity == 0) return MOE_OK;
+  return from_cuda(moe::launch_gemm_w2(hq, hs, offsets, E, I, d, w2, w2_sf, yp, rows_capacity,
+                                       static_cast<int*>(ws), stream));
+}
+
+moe_status moe_unpermute_combine(const uint16_t* yp, const int32_t* slot_to_row,
+                                 const float* topk_w, int32_t T, int32_t k, int32_t d,
+                                 uint16_t* y, cudaStream_t stream) {
+  if (T < 0 || k < 0) return MOE_ERR_INVALID_ARGUMENT;
+  moe_status s = check_width(d);
+  if (s != MOE_OK) return s;
+  if (k > kMaxK || int64_t(T) * k >= int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y || (k > 0 && (!yp || !slot_to_row || !topk_w))) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(y, 16) || (k > 0 && (!aligned(yp, 16) || !aligned(slot_to_row, 4) ||
+                                    !aligned(topk_w, 4))))
+    return MOE_ERR_INVALID_ARGUMENT;
+  return from_cuda(moe::launch_combine(yp, slot_to_row, topk_w, T, k, d, y, stream));
+}
+
+moe_status moe_workspace_size(const moe_dims* dims, int32_t pad_m, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARGUMENT;
+  moe_status s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  if (pad_m != kGemmPad) return MOE_ERR_UNSUPPORTED;
+  *bytes = forward_layout(*dims, pad_m).total;
+  return MOE_OK;
+}
+
+moe_status moe_forward(const moe_dims* dims, int32_t pad_m, const uint16_t* x,
+                       const float* logits, const moe_weights* W, uint16_t* y,
+                       int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  moe_status s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  if (pad_m != kGemmPad) return MOE_ERR_UNSUPPORTED;
+  const moe_dims D = *dims;
+  if (D.T == 0) return MOE_OK;
+  if (!x || !logits || !W || !y || !ws || !W->w13 || !W->w13_sf || !W->w2 || !W->w2_sf)
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(logits, 4) || !aligned(ws, 256) ||
+      !aligned(W->w13, 32) || !aligned(W->w2, 32) || !aligned(W->w13_sf, 16) ||
+      !aligned(W->w2_sf, 16) || (topk_ids_out && !aligned(topk_ids_out, 4)) ||
+      (topk_w_out && !aligned(topk_w_out, 4)))
+    return MOE_ERR_INVALID_ARGUMENT;
+  const ForwardLayout L = forward_layout(D, pad_m);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+
+  int* status = at<int>(ws, L.status);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (D.k == 0) return from_cuda(cudaMemsetAsync(y, 0, size_t(D.T) * D.d * 2, stream));
+
+  int* ids = topk_ids_out ? topk_ids_out : at<int>(ws, L.ids);
+  float* w = topk_w_out ? topk_w_out : at<float>(ws, L.w);
+  int* counts = at<int>(ws, L.counts);
+  int* offsets = at<int>(ws, L.offsets);
+  int* s2r = at<int>(ws, L.s2r);
+  int* r2s = at<int>(ws, L.r2s);
+  uint8_t* xq = at<uint8_t>(ws, L.xq);
+  uint8_t* xs = at<uint8_t>(ws, L.xs);
+  uint8_t* hq = at<uint8_t>(ws, L.hq);
+  uint8_t* hs = at<uint8_t>(ws, L.hs);
+  uint16_t* yp = at<uint16_t>(ws, L.yp);
+
+  if ((e = moe::launch_route_topk(logits, D.T, D.E, D.k, ids, w, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((e = moe::launch_permute(ids, D.T, D.E, D.k, pad_m, counts, offsets, s2r, r2s,
+                               at<int>(ws, L.hist), status, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((e = moe::launch_quant_mxfp8(x, D.T, D.d, s2r, D.k, xq, xs, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((e = moe::launch_gemm_w13_glu(xq, xs, offsets, D.E, D.d, D.I, W->w13, W->w13_sf, hq, hs,
+                                    L.rows_cap, status, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((e = moe::launch_gemm_w2(hq, hs, offsets, D.E, D.I, D.d, W->w2, W->w2_sf, yp, L.rows_cap,
+                               status, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return from_cuda(moe::launch_combine(yp, s2r, w, D.T, D.k, D.d, y, stream));
+}
+
+moe_status moe_check_device_status(const void* ws, cudaStream_t stream) {
+  if (!ws || !aligned(ws, 4)) return MOE_ERR_INVALID_ARGUMENT;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v < 0 || v > int(MOE_ERR_DEVICE_BAD_INPUT)) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(v);
+}
+
+moe_status moe_clear_device_status(void* ws, cudaStream_t stream) {
+  if (!ws || !aligned(ws, 4)) return MOE_ERR_INVALID_ARGUMENT;
+  return from_cuda(cudaMemsetAsync(ws, 0, sizeof(int), stream));
+}
+
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us,
+                                     cudaStream_t stream) {
+  if (!ws || !aligned(ws, 4)) return MOE_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < MOE_STATUS_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (limit_us == 0 || limit_us > 10u * 1000u * 1000u) return MOE_ERR_UNSUPPORTED;
+  return from_cuda(moe::launch_wait_timeout_selftest(static_cast<int*>(ws), limit_us, stream));
+}
+
+}  // extern "C"

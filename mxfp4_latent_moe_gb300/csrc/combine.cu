@@ -1,0 +1,61 @@
+// Routing-weighted combine: y[t] = bf16_rne(sum_j w[t][j] * Yp[slot_to_row[t*k+j]]).
+//
+// The layer ends with the weighted sum of the token's k expert outputs (the
+// routed-MoE layer of "Kimi K3.1 Pro at a glance"). One thread per 8 outputs
+// of a token: k 16-byte loads of grouped rows, fp32 fused multiply-adds in
+// j order, one 16-byte bf16 store. Every byte of y is written once, every
+// row of Yp is read once.
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kCombineThreads = 256;
+
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const uint4* __restrict__ yp, const int* __restrict__ slot_to_row,
+                   const float* __restrict__ w, int k, int d, uint4* __restrict__ y,
+                   int64_t total_vec) {
+  const int64_t g = int64_t(blockIdx.x) * kCombineThreads + threadIdx.x;
+  if (g >= total_vec) return;
+  const int vpr = d >> 3;
+  const int64_t t = g / vpr;
+  const int v = int(g - t * vpr);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const int64_t row = __ldg(slot_to_row + t * k + j);
+    const float wj = __ldg(w + t * k + j);
+    const uint4 q = __ldcs(yp + row * vpr + v);
+    const uint32_t q4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(wj, __uint_as_float(q4[i] << 16), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wj, __uint_as_float(q4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  y[g] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* yp, const int* slot_to_row, const float* w, int T,
+                           int k, int d, uint16_t* y, cudaStream_t st) {
+  const int64_t total = int64_t(T) * (d / 8);
+  if (total == 0) return cudaSuccess;
+  const int64_t blocks = (total + kCombineThreads - 1) / kCombineThreads;
+  combine_kernel<<<dim3(unsigned(blocks)), kCombineThreads, 0, st>>>(
+      reinterpret_cast<const uint4*>(yp), slot_to_row, w, k, d, reinterpret_cast<uint4*>(y),
+      total);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

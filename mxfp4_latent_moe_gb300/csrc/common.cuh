@@ -1,0 +1,259 @@
+// Device helpers shared by the libmoe kernels (sm_103a): status word, bounded
+// waits, the MX quantisation rule, and inline-PTX wrappers for mbarrier, TMA
+// (cp.async.bulk[.tensor]) and the 5th-generation tensor cores (tcgen05).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Device status word (first 4 bytes of every workspace). The first error wins.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Every spin-wait in these kernels gives up after this long and records
+// MOE_ERR_DEVICE_TIMEOUT instead of hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+// ---------------------------------------------------------------------------
+// MX rule (OCP MX v1.0) for MXFP8 = E4M3 elements + one E8M0 scale per 32.
+// ---------------------------------------------------------------------------
+
+// Scale code clamp(floor(log2(amax)) - 8 + 127, 0, 254); 0 for amax == 0.
+// floor(log2) is read exactly from the fp32 bit pattern (normal or subnormal).
+__device__ __forceinline__ int mx_scale_code(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  if (b == 0u) return 0;
+  const int field = int(b >> 23) & 0xFF;
+  const int fl = field ? field - 127 : (31 - __clz(int(b))) - 149;
+  const int code = fl - 8 + 127;
+  return code < 0 ? 0 : (code > 254 ? 254 : code);
+}
+
+// 2^(127 - code) as an fp32 (exact for code in [0, 253]; finite fp32 data
+// never gives a code above 246).
+__device__ __forceinline__ float mx_scale_mult(int code) {
+  return __uint_as_float(uint32_t(254 - code) << 23);
+}
+
+// Two fp32 -> two E4M3 codes (a in the low byte): round to nearest even,
+// saturate to +-448. Values far below the smallest subnormal are sent as a
+// signed zero so the sign of zero results never depends on the converter's
+// handling of fp32 subnormal inputs.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  a = fabsf(a) < 0x1p-11f ? copysignf(0.0f, a) : a;
+  b = fabsf(b) < 0x1p-11f ? copysignf(0.0f, b) : b;
+  return uint32_t(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Four scaled values -> four E4M3 codes packed little-endian.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d, float m) {
+  return e4m3x2(a * m, b * m) | (e4m3x2(c * m, d * m) << 16);
+}
+
+// Byte offset of the scale of row r, 32-block b in the TILED scale layout of
+// an operand with K inputs per row (K % 128 == 0): one 512-byte atom per 128
+// rows x 128 inputs; inside it row r sits at lane r%32, column (r/32)%4, byte
+// b%4 of the tensor-core scale-factor copy.
+__host__ __device__ __forceinline__ int64_t tiled_sf_offset(int64_t r, int64_t b, int64_t K) {
+  return ((r >> 7) * (K >> 7) + (b >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3);
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses, mbarriers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+// Waits until the phase with the given parity has completed. Gives up (returns
+// false) after limit_ns, or early when *abort becomes non-zero.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0u) {
+      if (abort && *abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA / bulk copies (global -> shared, completion counted on an mbarrier)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05: tensor memory, MMA, copies, loads
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrives once on `bar` when every tcgen05 operation this thread issued
+// before it has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// D(tmem) (+)= A(smem) x B(smem)^T with per-32 E8M0 scale factors in tmem.
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Copies a 32-row x 16-byte block from shared memory into tensor-memory
+// columns [taddr, taddr+4), replicated to all four 32-lane sub-partitions.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc)
+               : "memory");
+}
+
+// Each thread of the warp reads 32 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+      " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+      " [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): K-major operand written by
+// TMA with 128-byte swizzle, rows of 128 bytes, 8-row atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= uint64_t(1) << 16;                  // leading byte offset (unused here)
+  d |= uint64_t(1024 >> 4) << 32;          // stride byte offset: next 8-row atom
+  d |= uint64_t(1) << 46;                  // descriptor version (tcgen05)
+  d |= uint64_t(2) << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Descriptor of a scale-factor block: 32 rows x 16 bytes, no swizzle, 8-row
+// core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t desc_sf_block(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t(128 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 with E8M0 scales:
+// A/B formats (E4M3 = 0, E2M1 = 5), both K-major, dense, shape M x N.
+// The scale-factor ids (bits 4-5 for B, 29-30 for A) pick the byte of the
+// 32-bit scale column, i.e. which 32-input block of the stage the MMA uses.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(uint32_t a_fmt, uint32_t b_fmt, int M,
+                                                      int N) {
+  return (a_fmt << 7) | (b_fmt << 10) | (uint32_t(N >> 3) << 17) | (1u << 23) |
+         (uint32_t(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t id) {
+  return idesc | (id << 4) | (id << 29);
+}
+
+constexpr uint32_t kFmtE4M3 = 0;
+constexpr uint32_t kFmtE2M1 = 5;
+
+}  // namespace moe

@@ -1,0 +1,491 @@
+// Grouped GEMMs of the routed experts on tcgen05 block-scaled tensor cores.
+//
+// The pages' layer runs the routed experts through a grouped-MoE kernel with
+// MXFP4 weights and an FP8 second stage ("Kimi K3.1 Pro on AMD Instinct GPUs",
+// "The MXFP4 latent MoE on FlyDSL"; shapes from the Experts row of "Kimi K3.1
+// Pro at a glance": gate/up 3,584 -> 2 x 3,072, down 3,072 -> 3,584). Here:
+//
+//   stage 1 (MODE 0): [gate | up] = Xq . [W1 | W3]^T, h = silu(gate) * up,
+//                     h -> MXFP8 (E4M3 + E8M0 per 32) in the epilogue
+//   stage 2 (MODE 1): Yp = Hq . W2^T -> bf16
+//
+// Both are D[128 x 256] += A[128 x 128] . B[256 x 128]^T per pipeline stage,
+// with A = MXFP8 activations (E4M3) and B = MXFP4 weights (E2M1), one E8M0
+// scale per 32 inputs on each side, via tcgen05.mma kind::mxf8f6f4
+// (4 MMAs of K = 32 per stage, fp32 accumulators in tensor memory).
+//
+// CTA organisation (persistent, one CTA per SM, 192 threads):
+//   warp 0      TMA producer: A box 128x128 bytes, B box(es) of E2M1 expanded
+//               by TMA to one byte slot per element (16U4_ALIGN16B), both
+//               128-byte swizzled; the stage's scale atoms by bulk copy.
+//   warp 1      tensor-memory allocator + single-thread MMA issuer: copies the
+//               stage's scale atoms into tensor memory (tcgen05.cp), issues
+//               the 4 MMAs, frees the smem stage with tcgen05.commit.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one row per thread),
+//               fused GLU + MX requant (MODE 0) or bf16 conversion (MODE 1).
+// Tiles are (expert, n-tile, m-tile) with the m-tile fastest, so CTAs running
+// at the same time share one expert's weight tile through L2. The expert row
+// offsets are read on the device: no host synchronisation.
+// Every wait is bounded; on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT,
+// drains its outstanding copies and tensor-core work, frees tensor memory and
+// exits.
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;            // rows per tile (MMA M)
+constexpr int BK = 128;            // inputs per pipeline stage
+constexpr int BN = 256;            // MMA N
+constexpr int STAGES = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, 256)
+constexpr uint32_t kSfCol = 256;   // scale slots: 16 columns per stage (A: 4, B: 8)
+constexpr uint32_t A_BYTES = BM * BK;
+constexpr uint32_t B_BYTES = BN * BK;  // E2M1 in the 16-byte-aligned TMA expansion
+constexpr uint32_t SFA_BYTES = 512;
+constexpr uint32_t SFB_BYTES = 1024;
+constexpr uint32_t kStageTx = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + STAGES * A_BYTES;
+constexpr uint32_t kOffSfa = kOffB + STAGES * B_BYTES;
+constexpr uint32_t kOffSfb = kOffSfa + STAGES * SFA_BYTES;
+constexpr uint32_t kOffBars = kOffSfb + STAGES * SFB_BYTES;
+constexpr uint32_t kNumBars = 2 * STAGES + 3;  // full[S], empty[S], acc_full, acc_empty, drain
+constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
+constexpr uint32_t kOffSched = kOffMisc + 16;
+constexpr uint32_t kMaxE = 1024;
+constexpr uint32_t kSmemBytes = kOffSched + 2 * (kMaxE + 1) * 4 + 1024;
+
+struct GemmParams {
+  const uint8_t* a_sf;   // TILED scales of A
+  const uint8_t* b_sf;   // TILED scales of B
+  const int* offsets;    // [E+1]
+  int E;
+  int K;                 // inputs per row (d for MODE 0, I for MODE 1)
+  int I;                 // MODE 0: gate/up width; MODE 1: unused
+  int d;                 // MODE 1: output width; MODE 0: unused
+  int n_tiles;           // per expert
+  int64_t rows_capacity;
+  uint8_t* out_q;        // MODE 0: hq [rows][I]
+  uint8_t* out_sf;       // MODE 0: hs TILED (rows, I)
+  uint16_t* out_bf16;    // MODE 1: yp [rows][d]
+  int* status;
+};
+
+__device__ __forceinline__ void decode_tile(int tile, const int* prefix, const int* offs, int E,
+                                            int& e, int& nt, int& row0) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  e = lo;
+  const int r = tile - prefix[e];
+  const int mtiles = (offs[e + 1] - offs[e]) / BM;
+  nt = r / mtiles;
+  row0 = offs[e] + (r - nt * mtiles) * BM;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* total_holder = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  int* prefix = reinterpret_cast<int*>(smem + kOffSched);
+  int* offs = prefix + (kMaxE + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  const int KT = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4 * 32);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i <= E; i += kThreads) offs[i] = p.offsets[i];
+  __syncthreads();
+  if (warp == 0) {  // tile prefix over experts: lane owns a run of experts
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int s = 0;
+    bool bad = false;  // every group must be a non-negative multiple of BM rows
+    for (int e = e0; e < e1; ++e) {
+      const int rows = offs[e + 1] - offs[e];
+      bad |= rows < 0 || rows % BM != 0;
+      s += max(0, rows / BM) * p.n_tiles;
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    int incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += n;
+    }
+    int run = incl - s;
+    for (int e = e0; e < e1; ++e) {
+      prefix[e] = run;
+      run += max(0, (offs[e + 1] - offs[e]) / BM) * p.n_tiles;
+    }
+    if (lane == 31) {
+      const bool ok = !bad && offs[0] == 0 && int64_t(offs[E]) <= p.rows_capacity;
+      if (!ok && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE_BAD_INPUT);
+      prefix[E] = incl;
+      *total_holder = ok ? incl : 0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = *total_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t filled = 0, last_parity = 0;  // per-stage bits of the last fill
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        int e, nt, row0;
+        decode_tile(tile, prefix, offs, E, e, nt, row0);
+        bool failed = false;
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            failed = true;
+            break;
+          }
+          uint8_t* sa = smem + kOffA + stage * A_BYTES;
+          uint8_t* sb = smem + kOffB + stage * B_BYTES;
+          uint8_t* ssfa = smem + kOffSfa + stage * SFA_BYTES;
+          uint8_t* ssfb = smem + kOffSfb + stage * SFB_BYTES;
+          const uint8_t* gsfa = p.a_sf + (int64_t(row0 >> 7) * KT + kt) * 512;
+          if (MODE == 0) {
+            const int64_t g_row = int64_t(e) * 2 * p.I + int64_t(nt) * 128;
+            const int64_t u_row = g_row + p.I;
+            mbar_arrive_expect_tx(&full[stage], kStageTx);
+            tma_load_2d(sa, &tmap_a, &full[stage], kt * BK, row0);
+            tma_load_2d(sb, &tmap_b, &full[stage], kt * BK, int(g_row));
+            tma_load_2d(sb + B_BYTES / 2, &tmap_b, &full[stage], kt * BK, int(u_row));
+            bulk_load(ssfa, gsfa, SFA_BYTES, &full[stage]);
+            bulk_load(ssfb, p.b_sf + ((g_row >> 7) * KT + kt) * 512, 512, &full[stage]);
+            bulk_load(ssfb + 512, p.b_sf + ((u_row >> 7) * KT + kt) * 512, 512, &full[stage]);
+          } else {
+            const int64_t b_row = int64_t(e) * p.d + int64_t(nt) * BN;
+            const bool upper = nt * BN + 128 < p.d;
+            mbar_arrive_expect_tx(&full[stage], kStageTx - (upper ? 0u : 512u));
+            tma_load_2d(sa, &tmap_a, &full[stage], kt * BK, row0);
+            tma_load_2d(sb, &tmap_b, &full[stage], kt * BK, int(b_row));
+            bulk_load(ssfa, gsfa, SFA_BYTES, &full[stage]);
+            bulk_load(ssfb, p.b_sf + ((b_row >> 7) * KT + kt) * 512, 512, &full[stage]);
+            if (upper)
+              bulk_load(ssfb + 512, p.b_sf + (((b_row >> 7) + 1) * KT + kt) * 512, 512,
+                        &full[stage]);
+          }
+          filled |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (failed) {
+          *abort_flag = 1;
+          set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+          break;
+        }
+      }
+      // drain: every issued copy has landed before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if ((filled >> s) & 1u)
+          if (!mbar_wait(&full[s], (last_parity >> s) & 1u, nullptr))
+            set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_mxf8f6f4(kFmtE4M3, kFmtE2M1, BM, BN);
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      bool failed = false;
+      for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
+        if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + kOffA + stage * A_BYTES);
+          const uint32_t sb = smem_u32(smem + kOffB + stage * B_BYTES);
+          const uint32_t ssfa = smem_u32(smem + kOffSfa + stage * SFA_BYTES);
+          const uint32_t ssfb = smem_u32(smem + kOffSfb + stage * SFB_BYTES);
+          const uint32_t sfa_t = tmem_base + kSfCol + stage * 16;
+          const uint32_t sfb_t = sfa_t + 4;
+          tc_cp_32x128b_x4(sfa_t, desc_sf_block(ssfa));
+          tc_cp_32x128b_x4(sfb_t, desc_sf_block(ssfb));
+          tc_cp_32x128b_x4(sfb_t + 4, desc_sf_block(ssfb + 512));
+          const uint64_t adesc = desc_sw128_kmajor(sa);
+          const uint64_t bdesc = desc_sw128_kmajor(sb);
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            // +32 bytes along K inside the swizzle atom = +2 in the address field
+            tc_mma_mx(tmem_base + kAccCol, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk),
+                      idesc_with_sf_id(idesc, uint32_t(kk)), sfa_t, sfb_t,
+                      (kt > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (failed) break;
+        tc_commit(acc_full);
+        acc_phase ^= 1u;
+      }
+      if (failed) {
+        *abort_flag = 1;
+        set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+      }
+      // drain: all issued tensor-core work is complete before tensor memory is freed
+      tc_commit(drain);
+      if (!mbar_wait(drain, 0, nullptr)) set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // the tensor-memory lane quarter this warp may access
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, nt, row0;
+      decode_tile(tile, prefix, offs, E, e, nt, row0);
+      bool ok = mbar_wait(acc_full, acc_phase, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const int64_t row = int64_t(row0) + q * 32 + lane;
+      const uint32_t tq = tmem_base + kAccCol + (uint32_t(q * 32) << 16);
+      if (MODE == 0) {
+        uint32_t sword = 0;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld_32x32b_x32(tq + c * 32, g);
+          tmem_ld_32x32b_x32(tq + 128 + c * 32, u);
+          tmem_ld_wait();
+          float h[32];
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float gf = __uint_as_float(g[i]);
+            const float uf = __uint_as_float(u[i]);
+            h[i] = gf / (1.0f + expf(-gf)) * uf;
+            amax = fmaxf(amax, fabsf(h[i]));
+          }
+          const int code = mx_scale_code(amax);
+          const float m = mx_scale_mult(code);
+          uint4 o[2];
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            o[v].x = e4m3x4(h[16 * v + 0], h[16 * v + 1], h[16 * v + 2], h[16 * v + 3], m);
+            o[v].y = e4m3x4(h[16 * v + 4], h[16 * v + 5], h[16 * v + 6], h[16 * v + 7], m);
+            o[v].z = e4m3x4(h[16 * v + 8], h[16 * v + 9], h[16 * v + 10], h[16 * v + 11], m);
+            o[v].w = e4m3x4(h[16 * v + 12], h[16 * v + 13], h[16 * v + 14], h[16 * v + 15], m);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.out_q + row * p.I + int64_t(nt) * 128 + c * 32);
+          dst[0] = o[0];
+          dst[1] = o[1];
+          sword |= uint32_t(code) << (8 * c);
+        }
+        *reinterpret_cast<uint32_t*>(p.out_sf + tiled_sf_offset(row, int64_t(nt) * 4, p.I)) =
+            sword;
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col = nt * BN + c * 32;
+          if (col >= p.d) break;  // warp-uniform
+          uint32_t a[32];
+          tmem_ld_32x32b_x32(tq + c * 32, a);
+          tmem_ld_wait();
+          uint32_t o[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 b2 =
+                __floats2bfloat162_rn(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+            o[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + row * p.d + col);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// One CTA waits on a barrier that nothing signals; the bounded wait gives up
+// and records MOE_ERR_DEVICE_TIMEOUT.
+__global__ void wait_timeout_selftest_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait(&bar, 0, nullptr, limit_ns)) set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+// 2-D K-major operand map: dim0 = K inputs, dim1 = rows; 128-input boxes,
+// 128-byte swizzle.
+bool encode_operand(CUtensorMap* map, const void* base, bool e2m1, int K, int64_t rows,
+                    int box_rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(e2m1 ? K / 2 : K)};
+  const cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      fn(map, e2m1 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                        cudaStream_t st) {
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+  if (err != cudaSuccess) return err;
+  const int64_t max_tiles = (p.rows_capacity / BM) * p.n_tiles;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = int(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
+  grouped_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* offsets, int E,
+                                int d, int I, const uint8_t* w13, const uint8_t* w13_sf,
+                                uint8_t* hq, uint8_t* hs, int64_t rows_capacity, int* status,
+                                cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!encode_operand(&ta, xq, false, d, rows_capacity, BM)) return cudaErrorInvalidValue;
+  if (!encode_operand(&tb, w13, true, d, int64_t(E) * 2 * I, 128)) return cudaErrorInvalidValue;
+  GemmParams p{};
+  p.a_sf = xs;
+  p.b_sf = w13_sf;
+  p.offsets = offsets;
+  p.E = E;
+  p.K = d;
+  p.I = I;
+  p.d = d;
+  p.n_tiles = I / 128;
+  p.rows_capacity = rows_capacity;
+  p.out_q = hq;
+  p.out_sf = hs;
+  p.status = status;
+  return launch_mode<0>(p, ta, tb, st);
+}
+
+cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* offsets, int E, int I,
+                           int d, const uint8_t* w2, const uint8_t* w2_sf, uint16_t* yp,
+                           int64_t rows_capacity, int* status, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!encode_operand(&ta, hq, false, I, rows_capacity, BM)) return cudaErrorInvalidValue;
+  if (!encode_operand(&tb, w2, true, I, int64_t(E) * d, BN)) return cudaErrorInvalidValue;
+  GemmParams p{};
+  p.a_sf = hs;
+  p.b_sf = w2_sf;
+  p.offsets = offsets;
+  p.E = E;
+  p.K = I;
+  p.I = I;
+  p.d = d;
+  p.n_tiles = (d + BN - 1) / BN;
+  p.rows_capacity = rows_capacity;
+  p.out_bf16 = yp;
+  p.status = status;
+  return launch_mode<1>(p, ta, tb, st);
+}
+
+cudaError_t launch_wait_timeout_selftest(int* status, uint32_t limit_us, cudaStream_t st) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(status, uint64_t(limit_us) * 1000ull);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,34 @@
+// Launchers of the libmoe kernels (host side, C++ linkage, not exported).
+// Arguments are validated by the C-ABI layer (api.cu) before they get here.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int* ids, float* w,
+                              cudaStream_t st);
+
+size_t permute_scratch_bytes(int T, int E);
+cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* counts,
+                           int* offsets, int* slot_to_row, int* row_to_slot, int* hist,
+                           int* status, cudaStream_t st);
+
+cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
+                               uint8_t* codes, uint8_t* scales, cudaStream_t st);
+cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+                                  cudaStream_t st);
+
+cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* offsets, int E,
+                                int d, int I, const uint8_t* w13, const uint8_t* w13_sf,
+                                uint8_t* hq, uint8_t* hs, int64_t rows_capacity, int* status,
+                                cudaStream_t st);
+cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* offsets, int E, int I,
+                           int d, const uint8_t* w2, const uint8_t* w2_sf, uint16_t* yp,
+                           int64_t rows_capacity, int* status, cudaStream_t st);
+cudaError_t launch_wait_timeout_selftest(int* status, uint32_t limit_us, cudaStream_t st);
+
+cudaError_t launch_combine(const uint16_t* yp, const int* slot_to_row, const float* w, int T,
+                           int k, int d, uint16_t* y, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,159 @@
+// Expert grouping: histogram, exclusive scan of padded counts, stable scatter.
+//
+// The grouped-MoE kernel ("The MXFP4 latent MoE on FlyDSL") works on rows
+// grouped by expert. Rows of an expert follow ascending token order, so the
+// result is unique and independent of scheduling and of atomic ordering.
+//
+// Tokens are cut into chunks of 256 (one per block, 8 warps of 32 tokens).
+// Inside a chunk each warp builds, in shared memory, a 32-bit mask per expert
+// with bit `lane` set when the lane's token picked that expert. A token picks
+// an expert at most once, so a slot's rank among the chunk's slots of its
+// expert is popc(mask of lower lanes in its warp) + popc(masks of lower warps).
+//   1. permute_count:   per-chunk expert histograms hist[c][e]
+//   2. permute_scan:    counts, padded offsets, chunk bases (exclusive over c),
+//                       padding rows of row_to_slot set to -1
+//   3. permute_scatter: row = offsets[e] + base[c][e] + rank
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kChunk = 256;  // tokens per block
+constexpr int kWarps = kChunk / 32;
+
+// Builds the per-warp expert masks of one chunk. An id out of range or
+// repeated within a token records MOE_ERR_DEVICE_BAD_INPUT and is skipped
+// (no write ever leaves the expert's own rows).
+__device__ __forceinline__ void build_masks(const int* __restrict__ ids, int T, int E, int k,
+                                           uint32_t* masks, int* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) masks[i] = 0u;
+  __syncthreads();
+  const int t = blockIdx.x * kChunk + threadIdx.x;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[int64_t(t) * k + j];
+      if (e < 0 || e >= E) {
+        set_status(status, MOE_ERR_DEVICE_BAD_INPUT);
+        continue;
+      }
+      const uint32_t old = atomicOr(&masks[warp * E + e], 1u << lane);
+      if (old & (1u << lane)) set_status(status, MOE_ERR_DEVICE_BAD_INPUT);
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kChunk) permute_count_kernel(const int* __restrict__ ids,
+                                                               int T, int E, int k,
+                                                               int* __restrict__ hist,
+                                                               int* status) {
+  extern __shared__ uint32_t masks[];
+  build_masks(ids, T, E, k, masks, status);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += __popc(masks[w * E + e]);
+    hist[int64_t(blockIdx.x) * E + e] = s;
+  }
+}
+
+// One block of 1024 threads; E <= 1024.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int* __restrict__ hist, int C, int E,
+                                                            int pad_m, int* __restrict__ counts,
+                                                            int* __restrict__ offsets,
+                                                            int* __restrict__ row_to_slot) {
+  __shared__ int warp_sums[32];
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < E) {
+    for (int c = 0; c < C; ++c) {  // exclusive prefix over chunks, in place
+      const int v = hist[int64_t(c) * E + e];
+      hist[int64_t(c) * E + e] = cnt;
+      cnt += v;
+    }
+    counts[e] = cnt;
+  }
+  const int padded = e < E ? (cnt + pad_m - 1) / pad_m * pad_m : 0;
+  // block-wide exclusive scan of `padded`
+  const int lane = e & 31, warp = e >> 5;
+  int incl = padded;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += n;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+    int si = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, si, off);
+      if (lane >= off) si += n;
+    }
+    warp_sums[lane] = si - s;  // exclusive over warps
+  }
+  __syncthreads();
+  const int excl = incl - padded + warp_sums[warp];
+  if (e < E) {
+    offsets[e] = excl;
+    if (e == E - 1) offsets[E] = excl + padded;
+    for (int r = excl + cnt; r < excl + padded; ++r) row_to_slot[r] = -1;
+  }
+}
+
+__global__ void __launch_bounds__(kChunk) permute_scatter_kernel(
+    const int* __restrict__ ids, int T, int E, int k, const int* __restrict__ hist,
+    const int* __restrict__ offsets, int* __restrict__ slot_to_row, int* __restrict__ row_to_slot,
+    int* status) {
+  extern __shared__ uint32_t masks[];
+  build_masks(ids, T, E, k, masks, status);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kChunk + threadIdx.x;
+  if (t >= T) return;
+  const uint32_t lower = (1u << lane) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const int e = ids[int64_t(t) * k + j];
+    if (e < 0 || e >= E) continue;
+    int rank = __popc(masks[warp * E + e] & lower);
+    for (int w = 0; w < warp; ++w) rank += __popc(masks[w * E + e]);
+    const int row = offsets[e] + hist[int64_t(blockIdx.x) * E + e] + rank;
+    const int slot = t * k + j;
+    slot_to_row[slot] = row;
+    row_to_slot[row] = slot;
+  }
+}
+
+}  // namespace
+
+size_t permute_scratch_bytes(int T, int E) {
+  const size_t C = size_t((T + kChunk - 1) / kChunk);
+  return C * size_t(E) * sizeof(int);
+}
+
+cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* counts,
+                           int* offsets, int* slot_to_row, int* row_to_slot, int* hist,
+                           int* status, cudaStream_t st) {
+  const int C = (T + kChunk - 1) / kChunk;
+  const size_t smem = size_t(kWarps) * E * sizeof(uint32_t);
+  if (C > 0 && k > 0) {
+    permute_count_kernel<<<C, kChunk, smem, st>>>(ids, T, E, k, hist, status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  permute_scan_kernel<<<1, 1024, 0, st>>>(hist, (k > 0) ? C : 0, E, pad_m, counts, offsets,
+                                          row_to_slot);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (C > 0 && k > 0) {
+    permute_scatter_kernel<<<C, kChunk, smem, st>>>(ids, T, E, k, hist, offsets, slot_to_row,
+                                                    row_to_slot, status);
+    err = cudaGetLastError();
+  }
+  return err;
+}
+
+}  // namespace moe

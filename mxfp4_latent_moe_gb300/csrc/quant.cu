@@ -1,0 +1,111 @@
+// MXFP8 quantisation of the stage-1 activations and the one-time scale
+// prepack of the MXFP4 weights.
+//
+// MX rule (OCP MX v1.0; the pages' layer keeps its routed experts in MXFP4
+// with one E8M0 scale per 32 values and runs an FP8 second stage, "Kimi K3.1
+// Pro on AMD Instinct GPUs", "Kimi K3.1 Pro at a glance" and "The MXFP4 latent
+// MoE on FlyDSL"): per 32 consecutive values of a row the scale code is
+// clamp(floor(log2(amax)) - 8 + 127, 0, 254), and the elements are the E4M3
+// round-to-nearest-even of v * 2^(127 - code), saturated to +-448.
+//
+// Layout of the work: each thread owns 8 consecutive bf16 of one token (one
+// 16-byte load); 4 lanes share a 32-block (amax by two xor-shuffles) and 16
+// lanes a 128-input group whose four scale codes go out as one 32-bit word of
+// the TILED scale layout. The token is read once and written to each of its k
+// grouped rows (8-byte stores, 256 contiguous bytes per warp and row).
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kQuantThreads = 256;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_mxfp8_kernel(const uint4* __restrict__ x, int d, const int* __restrict__ slot_to_row,
+                       int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                       int64_t total_vec) {
+  const int64_t g = int64_t(blockIdx.x) * kQuantThreads + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const bool valid = g < total_vec;
+  const int vpr = d >> 3;  // 8-element vectors per row
+  uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+  if (valid) raw = __ldg(x + g);
+  float f[8];
+  bf16x8_to_f32(raw, f);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const int code = mx_scale_code(amax);
+  const float m = mx_scale_mult(code);
+  uint2 packed;
+  packed.x = e4m3x4(f[0], f[1], f[2], f[3], m);
+  packed.y = e4m3x4(f[4], f[5], f[6], f[7], m);
+  const int base = lane & ~15;
+  const uint32_t s0 = __shfl_sync(0xffffffffu, code, base);
+  const uint32_t s1 = __shfl_sync(0xffffffffu, code, base + 4);
+  const uint32_t s2 = __shfl_sync(0xffffffffu, code, base + 8);
+  const uint32_t s3 = __shfl_sync(0xffffffffu, code, base + 12);
+  if (!valid) return;
+  const uint32_t sword = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  const int64_t t = g / vpr;
+  const int v = int(g - t * vpr);
+  const int nrows = slot_to_row ? k : 1;
+  for (int j = 0; j < nrows; ++j) {
+    const int64_t row = slot_to_row ? int64_t(__ldg(slot_to_row + t * k + j)) : t;
+    *reinterpret_cast<uint2*>(codes + row * d + int64_t(v) * 8) = packed;
+    if ((lane & 15) == 0)
+      *reinterpret_cast<uint32_t*>(scales + tiled_sf_offset(row, int64_t(v >> 2), d)) = sword;
+  }
+}
+
+// canonical [rows][K/32] -> TILED; one thread per 32-bit output word.
+__global__ void prepack_scales_kernel(const uint8_t* __restrict__ src, int64_t rows, int K,
+                                      uint8_t* __restrict__ dst, int64_t words) {
+  const int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g >= words) return;
+  const int kt_count = K >> 7;
+  const int64_t r = g / kt_count;
+  const int kt = int(g - r * kt_count);
+  uint32_t w = 0;
+  if (r < rows) {
+    const uint8_t* p = src + r * (K >> 5) + kt * 4;
+    w = uint32_t(p[0]) | (uint32_t(p[1]) << 8) | (uint32_t(p[2]) << 16) | (uint32_t(p[3]) << 24);
+  }
+  *reinterpret_cast<uint32_t*>(dst + tiled_sf_offset(r, int64_t(kt) * 4, K)) = w;
+}
+
+}  // namespace
+
+cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
+                               uint8_t* codes, uint8_t* scales, cudaStream_t st) {
+  const int64_t total = int64_t(T) * (d / 8);
+  if (total == 0 || (slot_to_row && k == 0)) return cudaSuccess;
+  const int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
+  quant_mxfp8_kernel<<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
+      reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+                                  cudaStream_t st) {
+  const int64_t rows_p = (rows + 127) / 128 * 128;
+  const int64_t words = rows_p * (K / 128);
+  if (words == 0) return cudaSuccess;
+  const int64_t blocks = (words + 255) / 256;
+  prepack_scales_kernel<<<dim3(unsigned(blocks)), 256, 0, st>>>(src, rows, K, dst, words);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

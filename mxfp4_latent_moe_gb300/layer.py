@@ -1,0 +1,46 @@
+"""The MXFP4 latent-MoE layer as a Python object over the C-ABI.
+
+Holds the expert weights on the device (canonical packed E2M1 codes, scales
+prepacked once into the library's TILED layout) and calls moe_forward. Only
+allocation and argument marshalling happen here.
+"""
+import torch
+
+from . import abi
+
+
+class MoeLayer:
+    """Routed experts of one latent-MoE layer.
+
+    w13 u8 [E][2I][d/2] (gate rows, then up rows), w13_s u8 [E][2I][d/32],
+    w2 u8 [E][d][I/2], w2_s u8 [E][d][I/32], all CUDA tensors.
+    """
+
+    def __init__(self, w13, w13_s, w2, w2_s, k, pad_m=128, stream=None):
+        E, two_i, half_d = w13.shape
+        self.E, self.I, self.d, self.k, self.pad_m = E, two_i // 2, half_d * 2, k, pad_m
+        dev = w13.device
+        self.w13, self.w2 = w13.contiguous(), w2.contiguous()
+        self.w13_sf = torch.empty(abi.moe_tiled_scale_bytes(E * two_i, self.d), dtype=torch.uint8,
+                                  device=dev)
+        self.w2_sf = torch.empty(abi.moe_tiled_scale_bytes(E * self.d, self.I), dtype=torch.uint8,
+                                 device=dev)
+        abi.moe_prepack_scales(w13_s.contiguous(), E * two_i, self.d, self.w13_sf, stream)
+        abi.moe_prepack_scales(w2_s.contiguous(), E * self.d, self.I, self.w2_sf, stream)
+
+    def weight_bytes_per_expert(self):
+        return 3 * self.d * self.I // 2 + 3 * self.d * self.I // 32
+
+    def workspace(self, T):
+        n = abi.moe_workspace_size(T, self.d, self.E, self.k, self.I, self.pad_m)
+        return torch.empty(n, dtype=torch.uint8, device=self.w13.device)
+
+    def forward(self, x, logits, ws=None, y=None, topk_ids=None, topk_w=None, stream=None):
+        T = x.shape[0]
+        if ws is None:
+            ws = self.workspace(T)
+        if y is None:
+            y = torch.empty(T, self.d, dtype=torch.bfloat16, device=x.device)
+        abi.moe_forward(T, self.d, self.E, self.k, self.I, self.pad_m, x, logits, self.w13,
+                        self.w13_sf, self.w2, self.w2_sf, y, ws, topk_ids, topk_w, stream)
+        return y

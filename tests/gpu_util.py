@@ -1,0 +1,57 @@
+"""Helpers for the GPU parity tests: library loading, the TILED scale layout
+written out in numpy (from its definition in include/moe.h), tolerances."""
+import numpy as np
+import pytest
+import torch
+
+
+def cuda_lib():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for tests marked gpu")
+    from mxfp4_latent_moe_gb300 import abi
+    from mxfp4_latent_moe_gb300.build import build_library
+    build_library()
+    abi.lib()
+    return abi
+
+
+def tiled_index(rows, K):
+    """Byte offsets of scale (r, b) in the TILED layout, shape [rows][K/32]."""
+    r = np.arange(rows, dtype=np.int64)[:, None]
+    b = np.arange(K // 32, dtype=np.int64)[None, :]
+    return ((r // 128) * (K // 128) + b // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + b % 4
+
+
+def untile(tiled, rows, K):
+    flat = tiled.reshape(-1)
+    return flat[tiled_index(rows, K)]
+
+
+def tile(canon, K, rows_padded=None):
+    rows = canon.shape[0]
+    rp = rows_padded or (rows + 127) // 128 * 128
+    out = np.zeros(rp * (K // 32), np.uint8)
+    out[tiled_index(rows, K)] = canon
+    return out
+
+
+def e4m3(codes):
+    c = torch.from_numpy(np.ascontiguousarray(codes, np.uint8))
+    return c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def dequant_mxfp8(codes, scales):
+    return e4m3(codes) * np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=-1)
+
+
+def bf16_to_f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def assert_layer_close(got, ref, what="y"):
+    """The layer's output bar: |gpu - oracle| <= 2e-2 * rms(oracle row) + 1e-3."""
+    rms = np.sqrt((ref ** 2).mean(axis=-1, keepdims=True))
+    err = np.abs(got - ref)
+    bad = err > 2e-2 * rms + 1e-3
+    assert not bad.any(), "%s: %d of %d elements outside tolerance, worst %.3g (rms %.3g)" % (
+        what, int(bad.sum()), bad.size, float(err.max()), float(rms.max()))

@@ -1,0 +1,125 @@
+"""GPU parity of the whole layer (moe_forward, the call bench.py times)
+against the CPU oracle.
+
+Small shapes: every output element. The five workloads at full size, in the
+configuration the benchmark runs: routing bit-exact on every token, grouping
+bit-exact on every slot, MXFP8 codes of x bit-exact on sampled tokens (all
+outlier tokens included), and the bf16 output of sampled tokens within
+|gpu - oracle| <= 2e-2 * rms(oracle row) + 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_latent_moe_gb300 import synth
+from mxfp4_latent_moe_gb300.layer import MoeLayer
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def abi():
+    return gu.cuda_lib()
+
+
+def _run_forward(abi, wl, L):
+    layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k)
+    ws = layer.workspace(wl.T)
+    ids = torch.empty(wl.T, max(wl.k, 1), dtype=torch.int32, device="cuda")
+    w = torch.empty(wl.T, max(wl.k, 1), dtype=torch.float32, device="cuda")
+    y = layer.forward(L["x"], L["logits"], ws=ws, topk_ids=ids, topk_w=w)
+    assert abi.moe_check_device_status(ws) == 0
+    return y, ids[:, : wl.k], w[:, : wl.k]
+
+
+def _host_layer(L):
+    return {n: L[n].cpu().numpy() for n in ("w13", "w13_s", "w2", "w2_s")}
+
+
+@pytest.mark.parametrize("wl", [
+    synth.workload("tiny"),
+    synth.shape("ragged", T=200, d=512, E=40, k=6, I=384),
+    synth.shape("skewed", T=300, d=256, E=64, k=8, I=256, skew=True),
+    synth.shape("outliers", T=100, d=384, E=16, k=4, I=128, outlier_frac=0.05),
+    synth.shape("one_expert", T=130, d=256, E=1, k=1, I=256),
+    synth.shape("all_experts", T=20, d=128, E=8, k=8, I=128),
+])
+def test_forward_small_all_outputs(abi, orc, wl):
+    L = synth.make_layer(wl, seed=0, device="cuda")
+    y, ids, w = _run_forward(abi, wl, L)
+    H = _host_layer(L)
+    ref = orc.moe_forward(synth.bf16_bits(L["x"]), L["logits"].cpu().numpy(), wl.k, H["w13"],
+                          H["w13_s"], H["w2"], H["w2_s"], want_y64=True)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    np.testing.assert_allclose(w.cpu().numpy(), ref["w"], rtol=2e-6, atol=1e-7)
+    gu.assert_layer_close(gu.bf16_to_f64(y), ref["y64"])
+
+
+def test_forward_k0_gives_zeros_and_t0_is_a_noop(abi):
+    wl = synth.shape("k0", T=16, d=128, E=4, k=0, I=128)
+    L = synth.make_layer(wl, seed=0, device="cuda")
+    layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=0)
+    y = torch.full((16, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    layer.forward(L["x"], L["logits"], y=y)
+    torch.cuda.synchronize()
+    assert not y.float().abs().sum().item()
+    wl0 = synth.shape("t0", T=0, d=128, E=4, k=2, I=128)
+    L0 = synth.make_layer(wl0, seed=0, device="cuda")
+    layer0 = MoeLayer(L0["w13"], L0["w13_s"], L0["w2"], L0["w2_s"], k=2)
+    layer0.forward(L0["x"], L0["logits"], y=torch.empty(0, 128, dtype=torch.bfloat16,
+                                                        device="cuda"))
+    torch.cuda.synchronize()
+
+
+def _sample_tokens(wl, L, n):
+    g = np.random.default_rng(1234)
+    idx = set(g.choice(wl.T, size=min(n, wl.T), replace=False).tolist())
+    if wl.outlier_frac > 0:
+        amax = L["x"].float().abs().amax(dim=1).cpu().numpy()
+        out = np.argsort(-amax)[: int(round(wl.outlier_frac * wl.T))]
+        idx |= set(g.choice(out, size=min(8, len(out)), replace=False).tolist())
+    return np.array(sorted(idx))
+
+
+@pytest.mark.parametrize("name", ["decode_t64", "decode_t512", "prefill_skewed_t8192",
+                                  "prefill_outlier_t32768"])
+def test_forward_full_size_workloads(abi, orc, name):
+    wl = synth.workload(name)
+    L = synth.make_layer(wl, seed=0, device="cuda")
+    y, ids, w = _run_forward(abi, wl, L)
+    logits = L["logits"].cpu().numpy()
+    # routing: every token
+    rids, rw = orc.route_topk(logits, wl.k)
+    assert np.array_equal(ids.cpu().numpy(), rids)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
+    # grouping: every slot, through the step entry point
+    rc = abi.moe_rows_capacity(wl.T, wl.E, wl.k, 128)
+    counts = torch.empty(wl.E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(wl.E + 1, dtype=torch.int32, device="cuda")
+    s2r = torch.empty(wl.T * wl.k, dtype=torch.int32, device="cuda")
+    r2s = torch.empty(rc, dtype=torch.int32, device="cuda")
+    pws = torch.zeros(abi.moe_permute_workspace_size(wl.T, wl.E), dtype=torch.uint8, device="cuda")
+    abi.moe_permute(ids.contiguous(), wl.T, wl.E, wl.k, 128, counts, offsets, s2r, r2s, rc, pws)
+    assert abi.moe_check_device_status(pws) == 0
+    rperm = orc.permute(rids, wl.E, 128)
+    assert np.array_equal(offsets.cpu().numpy(), rperm["offsets"])
+    assert np.array_equal(s2r.cpu().numpy(), rperm["slot_to_row"])
+    # sampled tokens: MXFP8 codes of x at every grouped row, and the layer output
+    tok = _sample_tokens(wl, L, 24)
+    xq = torch.zeros(rc, wl.d, dtype=torch.uint8, device="cuda")
+    xs = torch.zeros(abi.moe_tiled_scale_bytes(rc, wl.d), dtype=torch.uint8, device="cuda")
+    abi.moe_quant_mxfp8(L["x"], wl.T, wl.d, s2r, wl.k, xq, xs, rc)
+    torch.cuda.synchronize()
+    xb = synth.bf16_bits(L["x"][torch.from_numpy(tok).cuda()])
+    ref_c, ref_s = orc.mx_quant_rows_bf16(xb)
+    rows = rperm["slot_to_row"].reshape(wl.T, wl.k)[tok]
+    xq_h = xq.cpu().numpy()
+    xs_h = gu.untile(xs.cpu().numpy(), rc, wl.d)
+    for j in range(wl.k):
+        assert np.array_equal(xq_h[rows[:, j]], ref_c)
+        assert np.array_equal(xs_h[rows[:, j]], ref_s)
+    H = _host_layer(L)
+    ref = orc.moe_forward(xb, logits[tok], wl.k, H["w13"], H["w13_s"], H["w2"], H["w2_s"],
+                          want_y64=True)
+    gu.assert_layer_close(gu.bf16_to_f64(y[torch.from_numpy(tok).cuda()]), ref["y64"], name)

@@ -1,0 +1,104 @@
+"""GPU parity of the two grouped GEMMs (tcgen05 block-scaled MMA) against the
+oracle's per-expert stage functions, on ragged expert groups: empty groups,
+groups of 1, 15..17, 127..129 and several hundred rows, K not a multiple of the
+pipeline depth, and more tiles than SMs."""
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_latent_moe_gb300 import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def abi():
+    return gu.cuda_lib()
+
+
+def _groups(sizes):
+    offsets = [0]
+    for c in sizes:
+        offsets.append(offsets[-1] + (c + 127) // 128 * 128)
+    rows = [(e, offsets[e] + i) for e, c in enumerate(sizes) for i in range(c)]
+    return np.array(offsets, np.int32), rows, max(offsets[-1], 128)
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _prepacked(abi, scales, rows, K):
+    dst = torch.empty(abi.moe_tiled_scale_bytes(rows, K), dtype=torch.uint8, device="cuda")
+    abi.moe_prepack_scales(_dev(scales.reshape(rows, K // 32)), rows, K, dst)
+    return dst
+
+
+def _check_mxfp8_rows(got_c, got_s, ref_c, ref_s):
+    """Codes of a requantised fp32 result: GPU (fp32 sums) vs oracle (fp64 sums
+    rounded to fp32). Codes may differ by one E4M3 step where the two sums
+    straddle a rounding boundary; scales by one where amax straddles a power
+    of two."""
+    assert np.all(np.abs(got_s.astype(int) - ref_s.astype(int)) <= 1)
+    assert (got_s != ref_s).mean() < 0.01
+    g = gu.dequant_mxfp8(got_c, got_s)
+    r = gu.dequant_mxfp8(ref_c, ref_s)
+    X = np.repeat(np.ldexp(1.0, np.maximum(got_s, ref_s).astype(int) - 127), 32, axis=-1)
+    step = np.maximum(np.abs(g), np.abs(r)) * 2.0 ** -3 + X * 2.0 ** -9
+    assert np.all(np.abs(g - r) <= step * 1.0001)
+    assert (got_c != ref_c).mean() < 0.01
+    rel = np.linalg.norm(g - r, axis=-1) / (np.linalg.norm(r, axis=-1) + 1e-300)
+    assert rel.max() < 0.02
+
+
+CASES = [
+    ([0, 1, 15, 16, 17, 127, 128, 129, 300], 256, 256),
+    ([3, 0, 250, 130], 384, 384),
+    (list(np.random.default_rng(0).integers(0, 300, 40)), 256, 512),
+]
+
+
+@pytest.mark.parametrize("sizes,d,I", CASES)
+def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I):
+    offsets, rows, rc = _groups(sizes)
+    E = len(sizes)
+    W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=1)
+    xq = synth.random_e4m3_codes((rc, d), seed=2).numpy()
+    xs = synth.random_scale_codes((rc, d // 32), lo=118, hi=130, seed=3).numpy()
+    hq = torch.zeros(rc, I, dtype=torch.uint8, device="cuda")
+    hs = torch.zeros(abi.moe_tiled_scale_bytes(rc, I), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    abi.moe_grouped_gemm_w13_glu(_dev(xq), _dev(gu.tile(xs, d)), _dev(offsets), E, d, I, 128,
+                                 W["w13"].cuda(), _prepacked(abi, W["w13_s"].numpy(), E * 2 * I, d),
+                                 hq, hs, rc, ws)
+    assert abi.moe_check_device_status(ws) == 0
+    got_c = hq.cpu().numpy()
+    got_s = gu.untile(hs.cpu().numpy(), rc, I)
+    w13, w13s = W["w13"].numpy(), W["w13_s"].numpy()
+    idx = [r for _, r in rows]
+    ref = np.stack([orc.expert_stage1(xq[r], xs[r], w13[e], w13s[e]) for e, r in rows])
+    ref_c, ref_s = orc.mx_quant_rows(ref.astype(np.float32))
+    _check_mxfp8_rows(got_c[idx], got_s[idx], ref_c, ref_s)
+
+
+@pytest.mark.parametrize("sizes,d,I", CASES)
+def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I):
+    offsets, rows, rc = _groups(sizes)
+    E = len(sizes)
+    W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=4)
+    hq = synth.random_e4m3_codes((rc, I), seed=5).numpy()
+    hs = synth.random_scale_codes((rc, I // 32), lo=118, hi=130, seed=6).numpy()
+    yp = torch.zeros(rc, d, dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    abi.moe_grouped_gemm_w2(_dev(hq), _dev(gu.tile(hs, I)), _dev(offsets), E, I, d, 128,
+                            W["w2"].cuda(), _prepacked(abi, W["w2_s"].numpy(), E * d, I), yp, rc,
+                            ws)
+    assert abi.moe_check_device_status(ws) == 0
+    got = gu.bf16_to_f64(yp)
+    w2, w2s = W["w2"].numpy(), W["w2_s"].numpy()
+    idx = [r for _, r in rows]
+    ref = np.stack([orc.expert_stage2(hq[r], hs[r], w2[e], w2s[e]) for e, r in rows])
+    rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
+    err = np.abs(got[idx] - ref)
+    assert np.all(err <= np.abs(ref) * 2.0 ** -8 + 1e-5 * rms), float((err / (rms + 1e-30)).max())
