@@ -44,10 +44,15 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, 256)
 constexpr uint32_t kSfCol = 256;   // scale slots: 16 columns per stage (A: 4, B: 8)
 constexpr uint32_t A_BYTES = BM * BK;
-constexpr uint32_t B_BYTES = BN * BK;  // E2M1 in the 16-byte-aligned TMA expansion
+// E2M1 in shared memory: TMA's 16U4_ALIGN16B expansion puts each 16 codes
+// (8 packed bytes) in the low half of a 16-byte slot, so a 128-input row takes
+// 128 bytes of shared memory; the mbarrier transaction count is the packed
+// size, half of that.
+constexpr uint32_t B_BYTES = BN * BK;
+constexpr uint32_t B_TX_BYTES = B_BYTES / 2;
 constexpr uint32_t SFA_BYTES = 512;
 constexpr uint32_t SFB_BYTES = 1024;
-constexpr uint32_t kStageTx = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr uint32_t kStageTx = A_BYTES + B_TX_BYTES + SFA_BYTES + SFB_BYTES;
 
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + STAGES * A_BYTES;
