@@ -1,0 +1,434 @@
+"""Benchmark of the MXFP4 latent-MoE layer on GB300 (one JSON line on rank 0).
+
+One step = one pass of the whole layer (route, group, quantise, stage-1 GEMM
++ GLU + requant, stage-2 GEMM, combine) over one batch of synthetic tokens of
+the chosen workload (default decode_t64: T=64, d=3584, E=896, k=16, I=3072).
+
+  value      tokens/s, device-timed with CUDA events around K moe_forward
+             calls, inputs resident in HBM (max over ranks; N ranks run
+             independent replicas of the workload).
+  e2e        the same metric through moe_forward with the step's inputs copied
+             from pinned host memory and the output read back, every step.
+  roofline   the dominant kernel: algorithmic bytes (HBM-bound workloads) or
+             FLOPs (tensor-bound) per launch / its mean event-timed duration,
+             against MEASURED_PEAKS.json.
+  cpu_baseline  the CPU oracle (test infrastructure) timed on the host cores on
+             a bounded sample of the same workload (rank 0, N=1 only).
+
+--impl reference runs the oracle itself as the reference arm.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s and % roofline (HBM GB/s decode, tensor TFLOP/s prefill), 1xGB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense ratio: kind::mxf8f6f4 runs at the FP8 rate
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_t64")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=0, help="oracle tokens (0 = automatic)")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, 1e30)
+        rows = [r for t, r in self.rows if t0 - 0.25 <= t <= t1 + 0.25] or [r for _, r in self.rows]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload, src_hash):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel source; None otherwise."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != src_hash:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def oracle_inputs(L, n_tokens):
+    """Host copies of the first n_tokens of the workload and of all weights."""
+    from mxfp4_latent_moe_gb300 import synth
+    xb = synth.bf16_bits(L["x"][:n_tokens])
+    lg = L["logits"][:n_tokens].cpu().numpy()
+    W = [L[n].cpu().numpy() for n in ("w13", "w13_s", "w2", "w2_s")]
+    return xb, lg, W
+
+
+def oracle_seconds(wl, host, threads):
+    """Time the CPU oracle, as it stands, on the prepared token sample."""
+    import oracle
+    xb, lg, W = host
+    t0 = time.perf_counter()
+    oracle.moe_forward(xb, lg, wl.k, *W, threads=threads)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from mxfp4_latent_moe_gb300 import synth
+    import oracle
+    oracle.build_oracle()
+    cores = os.cpu_count() or 1
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    L = synth.make_layer(wl, seed=args.seed, device=dev)
+    if args.cpu_sample:
+        n = args.cpu_sample
+    else:  # size the per-step sample so the whole run takes about 150 s
+        n0 = min(wl.T, cores)
+        per_token = oracle_seconds(wl, oracle_inputs(L, n0), cores) / n0
+        n = max(1, min(wl.T, int(150.0 / (args.steps + args.warmup) / per_token)))
+    host = oracle_inputs(L, n)
+    del L
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = oracle_seconds(wl, host, cores)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = n * len(times) / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "first %d tokens of the workload per step, full layer" % n},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    from mxfp4_latent_moe_gb300 import synth
+    wl = synth.workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_latent_moe_gb300 import abi
+    from mxfp4_latent_moe_gb300.layer import MoeLayer
+
+    L = synth.make_layer(wl, seed=args.seed + rank, device=dev)
+    layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k)
+    T, d, E, k, I = wl.T, wl.d, wl.E, wl.k, wl.I
+    x, logits = L["x"], L["logits"]
+    ws = layer.workspace(T)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        layer.forward(x, logits, ws=ws, y=y, topk_ids=ids, topk_w=w)
+
+    # routing statistics for the roofline (outside any timed region)
+    fwd()
+    if abi.moe_check_device_status(ws) != abi.OK:
+        raise RuntimeError("device status error in the first forward")
+    counts = torch.bincount(ids.reshape(-1).long(), minlength=E)
+    U = int((counts > 0).sum())
+    valid_rows = T * k
+    rows_cap = abi.moe_rows_capacity(T, E, k, 128)
+    padded_rows = int(((counts + 127) // 128 * 128).sum())
+    expert_bytes = layer.weight_bytes_per_expert()
+    w13_bytes = 2 * I * d // 2 + 2 * I * d // 32
+    w2_bytes = d * I // 2 + d * I // 32
+    flops = 6.0 * T * k * d * I
+    l2_note = "inputs larger than L2 (touched weights %.2f GB)" % (U * expert_bytes / 1e9)
+    flush = None
+    if U * expert_bytes < 512e6:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        l2_note = "L2 flushed between steps (256 MB write)"
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(max(3, args.warmup)):
+        fwd()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K moe_forward calls on device-resident inputs
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.mark()
+    if flush is None:
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            fwd()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        total_ms = t_start.elapsed_time(t_end)
+    else:  # time each step between its L2 flush and the next
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[2 * i].record(stream)
+            fwd()
+            ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        total_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps))
+    sampler.mark()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        torch.distributed.barrier()
+    launches_per_step = 8
+
+    # ---- per-kernel breakdown: the same kernels through the step entry points
+    rc = rows_cap
+    counts_d = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets_d = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    s2r = torch.empty(T * k, dtype=torch.int32, device=dev)
+    r2s = torch.empty(rc, dtype=torch.int32, device=dev)
+    pws = torch.zeros(abi.moe_permute_workspace_size(T, E), dtype=torch.uint8, device=dev)
+    xq = torch.empty(rc, d, dtype=torch.uint8, device=dev)
+    xs = torch.empty(abi.moe_tiled_scale_bytes(rc, d), dtype=torch.uint8, device=dev)
+    hq = torch.empty(rc, I, dtype=torch.uint8, device=dev)
+    hs = torch.empty(abi.moe_tiled_scale_bytes(rc, I), dtype=torch.uint8, device=dev)
+    yp = torch.empty(rc, d, dtype=torch.bfloat16, device=dev)
+    gws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    names = ["route_topk", "permute", "quant_mxfp8", "gemm_w13_glu", "gemm_w2", "combine"]
+    calls = [
+        lambda: abi.moe_route_topk(logits, T, E, k, ids, w),
+        lambda: abi.moe_permute(ids, T, E, k, 128, counts_d, offsets_d, s2r, r2s, rc, pws),
+        lambda: abi.moe_quant_mxfp8(x, T, d, s2r, k, xq, xs, rc),
+        lambda: abi.moe_grouped_gemm_w13_glu(xq, xs, offsets_d, E, d, I, 128, layer.w13,
+                                             layer.w13_sf, hq, hs, rc, gws),
+        lambda: abi.moe_grouped_gemm_w2(hq, hs, offsets_d, E, I, d, 128, layer.w2, layer.w2_sf,
+                                        yp, rc, gws),
+        lambda: abi.moe_unpermute_combine(yp, s2r, w, T, k, d, y),
+    ]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+           for _ in range(args.steps)]
+    for i in range(max(3, args.warmup // 2)):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        kev[i][0].record(stream)
+        for j, c in enumerate(calls):
+            c()
+            kev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark()
+    kms = {n: statistics.mean(kev[i][j].elapsed_time(kev[i][j + 1]) for i in range(args.steps))
+           for j, n in enumerate(names)}
+    if abi.moe_check_device_status(gws) != abi.OK or abi.moe_check_device_status(pws) != abi.OK:
+        raise RuntimeError("device status error in the kernel breakdown")
+
+    # ---- end to end through the public API: pinned host in, host out, every step
+    x_h = x.cpu().pin_memory()
+    lg_h = logits.cpu().pin_memory()
+    y_h = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    lg_d = torch.empty_like(logits)
+    for _ in range(3):
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        layer.forward(x_d, lg_d, ws=ws, y=y)
+        y_h.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        layer.forward(x_d, lg_d, ws=ws, y=y)
+        y_h.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peaks, peak_src = load_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * FP8_OVER_BF16
+    t_mem = U * expert_bytes / (hbm_peak * 1e9)
+    t_math = flops / (tensor_peak * 1e12)
+    bound = "hbm" if t_mem >= t_math else "tensor"
+    ms_per_step = total_ms / args.steps
+    layer_frac = max(t_mem, t_math) / (ms_per_step / 1e3)
+    src_hash = source_hash(["mxfp4_latent_moe_gb300/csrc/gemm.cu",
+                            "mxfp4_latent_moe_gb300/csrc/common.cuh"])
+    dom = "gemm_w13_glu"
+    dom_s = kms[dom] / 1e3
+    if bound == "hbm":
+        dom_bytes = U * w13_bytes + valid_rows * (d + d // 32) + valid_rows * (I + I // 32)
+        roof = {"kernel": dom, "bound": "hbm", "achieved": dom_bytes / dom_s / 1e9,
+                "peak": hbm_peak, "unit": "GB/s", "frac": dom_bytes / dom_s / 1e9 / hbm_peak,
+                "traffic": profiled_traffic(dom, wl.name, src_hash),
+                "algorithmic_bytes": dom_bytes, "peak_source": peak_src}
+    else:
+        dom_flops = 4.0 * T * k * d * I
+        roof = {"kernel": dom, "bound": "tensor", "achieved": dom_flops / dom_s / 1e12,
+                "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": dom_flops / dom_s / 1e12 / tensor_peak,
+                "traffic": profiled_traffic(dom, wl.name, src_hash),
+                "algorithmic_flops": dom_flops,
+                "peak_source": peak_src + " bf16 x %.1f (fp8 / bf16 nominal ratio)" % FP8_OVER_BF16}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_sample or (T if T <= 64 else 32)
+        cores = os.cpu_count() or 1
+        dt = oracle_seconds(wl, oracle_inputs(L, n), cores)
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": "first %d of %d tokens, full layer (%.1f s)" % (n, T, dt)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": world * T * args.steps / (total_ms / 1e3),
+            "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "mxfp8(e4m3)xmxfp4(e2m1)->f32",
+            "data": "synthetic (seeded; x~N(0,1) bf16, logits~N(0,1), uniform E2M1 codes, "
+                    "E8M0 scales 118..122)",
+            "config": {"workload": wl.name, "T": T, "d": d, "E": E, "k": k, "I": I,
+                       "pad_m": 128, "touched_experts": U, "padded_rows": padded_rows,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": l2_note},
+            "layer_roofline": {"bound": bound, "time_ms": 1e3 * max(t_mem, t_math),
+                               "frac": layer_frac, "tflops": flops / (ms_per_step / 1e3) / 1e12,
+                               "weight_gbs": U * expert_bytes / (ms_per_step / 1e3) / 1e9},
+            "roofline": roof,
+            "kernels_ms": kms,
+            "gpu_launches": launches_per_step * args.steps,
+            "e2e": {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * d * 2 + T * E * 4,
+                    "d2h_bytes_per_step": T * d * 2},
+            "cpu_baseline": cpu,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -50,7 +50,13 @@ WORKLOADS = [
     Workload("prefill_outlier_t32768", T=32768, d=3584, E=896, k=16, I=3072,
              outlier_frac=0.01),
 ]
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Reduced cases of the same kernels for profiler captures (about 1 GB of
+# weights, still far larger than the 129 MB L2): full d and I, 64 experts.
+PROFILE_WORKLOADS = [
+    Workload("ncu_decode_t64_e64", T=64, d=3584, E=64, k=16, I=3072),
+    Workload("ncu_prefill_t2048_e64", T=2048, d=3584, E=64, k=16, I=3072),
+]
+BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS}
 
 
 def workload(name_or_index):
