@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=0, help="oracle tokens (0 = automatic)")
+    ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "token", "weight"],
+                    help="grouped-GEMM family (auto = the library's default for the shape)")
     return ap.parse_args()
 
 
@@ -222,7 +224,9 @@ def main():
     from mxfp4_latent_moe_gb300.layer import MoeLayer
 
     L = synth.make_layer(wl, seed=args.seed + rank, device=dev)
-    layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k)
+    kernel_arg = {"auto": abi.GEMM_AUTO, "token": abi.GEMM_TOKEN_TILES,
+                  "weight": abi.GEMM_WEIGHT_TILES}[args.gemm_kernel]
+    layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k, kernel=kernel_arg)
     T, d, E, k, I = wl.T, wl.d, wl.E, wl.k, wl.I
     x, logits = L["x"], L["logits"]
     ws = layer.workspace(T)
@@ -242,6 +246,7 @@ def main():
     U = int((counts > 0).sum())
     valid_rows = T * k
     rows_cap = abi.moe_rows_capacity(T, E, k, 128)
+    kernel = layer.kernel_for(T)
     padded_rows = int(((counts + 127) // 128 * 128).sum())
     expert_bytes = layer.weight_bytes_per_expert()
     w13_bytes = 2 * I * d // 2 + 2 * I * d // 32
@@ -307,10 +312,10 @@ def main():
         lambda: abi.moe_route_topk(logits, T, E, k, ids, w),
         lambda: abi.moe_permute(ids, T, E, k, 128, counts_d, offsets_d, s2r, r2s, rc, pws),
         lambda: abi.moe_quant_mxfp8(x, T, d, s2r, k, xq, xs, rc),
-        lambda: abi.moe_grouped_gemm_w13_glu(xq, xs, offsets_d, E, d, I, 128, layer.w13,
-                                             layer.w13_sf, hq, hs, rc, gws),
-        lambda: abi.moe_grouped_gemm_w2(hq, hs, offsets_d, E, I, d, 128, layer.w2, layer.w2_sf,
-                                        yp, rc, gws),
+        lambda: abi.moe_grouped_gemm_w13_glu(xq, xs, counts_d, offsets_d, E, d, I, kernel,
+                                             layer.w13, layer.w13_sf, hq, hs, rc, gws),
+        lambda: abi.moe_grouped_gemm_w2(hq, hs, counts_d, offsets_d, E, I, d, kernel, layer.w2,
+                                        layer.w2_sf, yp, rc, gws),
         lambda: abi.moe_unpermute_combine(yp, s2r, w, T, k, d, y),
     ]
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
@@ -410,7 +415,8 @@ def main():
             "data": "synthetic (seeded; x~N(0,1) bf16, logits~N(0,1), uniform E2M1 codes, "
                     "E8M0 scales 118..122)",
             "config": {"workload": wl.name, "T": T, "d": d, "E": E, "k": k, "I": I,
-                       "pad_m": 128, "touched_experts": U, "padded_rows": padded_rows,
+                       "gemm_kernel": "weight_tiles" if kernel == abi.GEMM_WEIGHT_TILES
+                       else "token_tiles", "touched_experts": U, "padded_rows": padded_rows,
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": l2_note},
             "layer_roofline": {"bound": bound, "time_ms": 1e3 * max(t_mem, t_math),

@@ -36,8 +36,18 @@
  * Shapes (checked; anything else is MOE_ERR_UNSUPPORTED):
  *   1 <= E <= 1024, 0 <= k <= min(E, 32), T >= 0, T*k < 2^31,
  *   d % 128 == 0 and I % 128 == 0 (both >= 128),
- *   pad_m == 128 for the grouped GEMMs and moe_forward; moe_permute takes any
- *   power of two 1..1024.
+ *   grouped GEMMs and moe_forward: expert groups padded to 128 rows
+ *   (moe_permute with pad_m = 128); moe_permute itself takes any power of two
+ *   1..1024.
+ *
+ * Two kernel families run the grouped GEMMs (moe_gemm_kernel):
+ *   MOE_GEMM_TOKEN_TILES   tokens are the MMA's M side (128-row tiles),
+ *                          weights the N side; for many tokens per expert.
+ *   MOE_GEMM_WEIGHT_TILES  weights are the M side (128 weight rows per MMA),
+ *                          an expert's tokens the N side (its count rounded up
+ *                          to 32, at most 128 per tile); for a few tokens per
+ *                          expert (decode), where streaming the weights from
+ *                          HBM is the bound.
  *
  * Data layouts:
  *   x, y        bf16 [T][d] row-major.
@@ -80,6 +90,12 @@ typedef enum {
   MOE_ERR_DEVICE_BAD_INPUT = 6     /* device status: expert id out of range or repeated */
 } moe_status;
 
+typedef enum {
+  MOE_GEMM_AUTO = 0,         /* moe_forward only: see moe_default_kernel */
+  MOE_GEMM_TOKEN_TILES = 1,  /* tokens on the MMA's M side */
+  MOE_GEMM_WEIGHT_TILES = 2  /* weights on the MMA's M side, tokens as N */
+} moe_gemm_kernel;
+
 typedef struct {
   int32_t T; /* tokens */
   int32_t d; /* latent width (3584) */
@@ -108,6 +124,11 @@ int32_t moe_abi_version(void);
  * to a multiple of 128). Returns 0 for unsupported K. */
 size_t moe_tiled_scale_bytes(int64_t rows, int32_t K);
 
+/* The GEMM kernels moe_forward uses for MOE_GEMM_AUTO: MOE_GEMM_WEIGHT_TILES
+ * while T*k < 64*E (fewer than 64 tokens per expert on average), else
+ * MOE_GEMM_TOKEN_TILES. Returns -1 for an unsupported shape. */
+int32_t moe_default_kernel(int32_t T, int32_t E, int32_t k);
+
 /* Rows a grouped activation buffer needs for T tokens, k experts each, E
  * experts and padding pad_m: T*k + min(E, T*k)*(pad_m-1), rounded up to 128. */
 int64_t moe_rows_capacity(int32_t T, int32_t E, int32_t k, int32_t pad_m);
@@ -135,7 +156,8 @@ size_t moe_permute_workspace_size(int32_t T, int32_t E);
  * FlyDSL"): histogram, exclusive scan of padded counts, stable scatter.
  * counts [E]; offsets [E+1] with offsets[e+1] = offsets[e] +
  * ceil(counts[e]/pad_m)*pad_m; slot_to_row [T*k]; row_to_slot [rows_capacity]
- * (slot of each grouped row, -1 on padding rows, untouched past offsets[E]).
+ * (slot of each grouped row; -1 on every row of [0, rows_capacity) that holds
+ * no slot, padding rows included).
  * Within an expert, rows follow ascending token order: the result is unique
  * and does not depend on scheduling. rows_capacity must be at least
  * moe_rows_capacity(T, E, k, pad_m) (checked on the host). An id out of range
@@ -163,28 +185,35 @@ moe_status moe_quant_mxfp8(const uint16_t* x, int32_t T, int32_t d, const int32_
  * (kind::mxf8f6f4, MXFP8 activations x MXFP4 weights, fp32 accumulation)
  * with the GLU and the FP8 second-stage quantisation fused in the epilogue
  * ("The MXFP4 latent MoE on FlyDSL"; expert shapes from the Experts row).
- * For each expert e and each grouped row r in [offsets[e], offsets[e+1]):
+ * For each expert e and each of its grouped rows r:
  *   g = X[r] . W1[e]^T, u = X[r] . W3[e]^T  (dequantised operands, fp32 sums)
  *   h = silu(g) * u (fp32), then MXFP8 as in moe_quant_mxfp8
  *   -> hq [r][I] codes and hs TILED scales for (rows_capacity, I).
- * offsets int32 [E+1] is read on the device; offsets[E] <= rows_capacity and
- * offsets[e] % pad_m == 0 are the caller's (moe_permute's) guarantee.
+ * counts int32 [E] and offsets int32 [E+1] are read on the device and must
+ * come from moe_permute with pad_m = 128: every group a multiple of 128 rows
+ * holding counts[e] tokens, offsets[0] == 0, offsets[E] <= rows_capacity.
+ * Offsets or counts that break this are refused on the device
+ * (MOE_ERR_DEVICE_BAD_INPUT in the status word, nothing written).
+ * MOE_GEMM_TOKEN_TILES computes every row of each group (padding rows hold
+ * unspecified values); MOE_GEMM_WEIGHT_TILES computes the first counts[e]
+ * rows rounded up to 32 and leaves the rest untouched.
+ * kernel: MOE_GEMM_TOKEN_TILES or MOE_GEMM_WEIGHT_TILES.
  * ws: at least MOE_STATUS_BYTES; the status word records timeouts.
  * xq, hq 16-byte aligned; w13 32-byte aligned; scale arrays 16-byte aligned. */
-moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets,
-                                    int32_t E, int32_t d, int32_t I, int32_t pad_m,
-                                    const uint8_t* w13, const uint8_t* w13_sf, uint8_t* hq,
-                                    uint8_t* hs, int64_t rows_capacity, void* ws,
+moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int32_t* counts,
+                                    const int32_t* offsets, int32_t E, int32_t d, int32_t I,
+                                    int32_t kernel, const uint8_t* w13, const uint8_t* w13_sf,
+                                    uint8_t* hq, uint8_t* hs, int64_t rows_capacity, void* ws,
                                     size_t ws_bytes, cudaStream_t stream);
 
 /* Stage 2 grouped GEMM (the down projection w2, 3,072 -> 3,584 in the pages'
  * layer): Yp[r] = H[r] . W2[e]^T with MXFP8 H and MXFP4 W2 on tcgen05
  * block-scaled tensor cores, fp32 accumulation, rounded to bf16.
  * yp bf16 [rows_capacity][d], 16-byte aligned. Other arguments as above. */
-moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32_t* offsets,
-                               int32_t E, int32_t I, int32_t d, int32_t pad_m,
-                               const uint8_t* w2, const uint8_t* w2_sf, uint16_t* yp,
-                               int64_t rows_capacity, void* ws, size_t ws_bytes,
+moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32_t* counts,
+                               const int32_t* offsets, int32_t E, int32_t I, int32_t d,
+                               int32_t kernel, const uint8_t* w2, const uint8_t* w2_sf,
+                               uint16_t* yp, int64_t rows_capacity, void* ws, size_t ws_bytes,
                                cudaStream_t stream);
 
 /* Routing-weighted combine: y[t] = bf16_rne(sum_{j=0..k-1} topk_w[t][j] *
@@ -194,16 +223,17 @@ moe_status moe_unpermute_combine(const uint16_t* yp, const int32_t* slot_to_row,
                                  const float* topk_w, int32_t T, int32_t k, int32_t d,
                                  uint16_t* y, cudaStream_t stream);
 
-/* Workspace bytes moe_forward needs for these dims and pad_m. */
-moe_status moe_workspace_size(const moe_dims* dims, int32_t pad_m, size_t* bytes);
+/* Workspace bytes moe_forward needs for these dims. */
+moe_status moe_workspace_size(const moe_dims* dims, size_t* bytes);
 
 /* The whole layer: route -> permute -> quantise -> stage-1 GEMM + GLU +
  * requant -> stage-2 GEMM -> combine, all on `stream` with no host
- * synchronisation. Clears the status word at its start.
+ * synchronisation. Clears the status word at its start. kernel selects the
+ * grouped-GEMM family (moe_gemm_kernel; MOE_GEMM_AUTO = moe_default_kernel).
  * x bf16 [T][d], logits fp32 [T][E], weights as in moe_weights, y bf16 [T][d].
  * topk_ids_out / topk_w_out may be NULL; if given they receive the routing.
  * ws: moe_workspace_size bytes, 256-byte aligned. */
-moe_status moe_forward(const moe_dims* dims, int32_t pad_m, const uint16_t* x,
+moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
                        const float* logits, const moe_weights* weights, uint16_t* y,
                        int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
                        cudaStream_t stream);

@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 
 STATUS_BYTES = 256
 OK, INVALID_ARGUMENT, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA, DEVICE_TIMEOUT, DEVICE_BAD_INPUT = range(7)
+GEMM_AUTO, GEMM_TOKEN_TILES, GEMM_WEIGHT_TILES = range(3)
 
 
 class MoeError(RuntimeError):
@@ -42,17 +43,18 @@ _SIGS = {
     "moe_abi_version": (_i32, []),
     "moe_tiled_scale_bytes": (_sz, [_i64, _i32]),
     "moe_rows_capacity": (_i64, [_i32, _i32, _i32, _i32]),
+    "moe_default_kernel": (_i32, [_i32, _i32, _i32]),
     "moe_prepack_scales": (_i32, [_vp, _i64, _i32, _vp, _vp]),
     "moe_route_topk": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_permute_workspace_size": (_sz, [_i32, _i32]),
     "moe_permute": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
     "moe_quant_mxfp8": (_i32, [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _i64, _vp]),
-    "moe_grouped_gemm_w13_glu": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
-                                        _i64, _vp, _sz, _vp]),
-    "moe_grouped_gemm_w2": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i64, _vp,
-                                   _sz, _vp]),
+    "moe_grouped_gemm_w13_glu": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
+                                        _vp, _i64, _vp, _sz, _vp]),
+    "moe_grouped_gemm_w2": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i64,
+                                   _vp, _sz, _vp]),
     "moe_unpermute_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]),
-    "moe_workspace_size": (_i32, [ctypes.POINTER(_Dims), _i32, ctypes.POINTER(_sz)]),
+    "moe_workspace_size": (_i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_sz)]),
     "moe_forward": (_i32, [ctypes.POINTER(_Dims), _i32, _vp, _vp, ctypes.POINTER(_Weights), _vp,
                            _vp, _vp, _vp, _sz, _vp]),
     "moe_check_device_status": (_i32, [_vp, _vp]),
@@ -123,13 +125,17 @@ def moe_rows_capacity(T, E, k, pad_m):
     return lib().moe_rows_capacity(T, E, k, pad_m)
 
 
+def moe_default_kernel(T, E, k):
+    return lib().moe_default_kernel(T, E, k)
+
+
 def moe_permute_workspace_size(T, E):
     return lib().moe_permute_workspace_size(T, E)
 
 
-def moe_workspace_size(T, d, E, k, I, pad_m=128):
+def moe_workspace_size(T, d, E, k, I):
     out = _sz(0)
-    _check("moe_workspace_size", lib().moe_workspace_size(ctypes.byref(_Dims(T, d, E, k, I)), pad_m,
+    _check("moe_workspace_size", lib().moe_workspace_size(ctypes.byref(_Dims(T, d, E, k, I)),
                                                           ctypes.byref(out)))
     return out.value
 
@@ -156,17 +162,17 @@ def moe_quant_mxfp8(x, T, d, slot_to_row, k, codes, scales, rows_capacity, strea
           rows_capacity, _stream(stream))
 
 
-def moe_grouped_gemm_w13_glu(xq, xs, offsets, E, d, I, pad_m, w13, w13_sf, hq, hs, rows_capacity,
-                             ws, stream=None):
-    _call("moe_grouped_gemm_w13_glu", _ptr(xq), _ptr(xs), _ptr(offsets), E, d, I, pad_m, _ptr(w13),
-          _ptr(w13_sf), _ptr(hq), _ptr(hs), rows_capacity, _ptr(ws),
+def moe_grouped_gemm_w13_glu(xq, xs, counts, offsets, E, d, I, kernel, w13, w13_sf, hq, hs,
+                             rows_capacity, ws, stream=None):
+    _call("moe_grouped_gemm_w13_glu", _ptr(xq), _ptr(xs), _ptr(counts), _ptr(offsets), E, d, I,
+          kernel, _ptr(w13), _ptr(w13_sf), _ptr(hq), _ptr(hs), rows_capacity, _ptr(ws),
           ws.numel() * ws.element_size(), _stream(stream))
 
 
-def moe_grouped_gemm_w2(hq, hs, offsets, E, I, d, pad_m, w2, w2_sf, yp, rows_capacity, ws,
+def moe_grouped_gemm_w2(hq, hs, counts, offsets, E, I, d, kernel, w2, w2_sf, yp, rows_capacity, ws,
                         stream=None):
-    _call("moe_grouped_gemm_w2", _ptr(hq), _ptr(hs), _ptr(offsets), E, I, d, pad_m, _ptr(w2),
-          _ptr(w2_sf), _ptr(yp), rows_capacity, _ptr(ws), ws.numel() * ws.element_size(),
+    _call("moe_grouped_gemm_w2", _ptr(hq), _ptr(hs), _ptr(counts), _ptr(offsets), E, I, d, kernel,
+          _ptr(w2), _ptr(w2_sf), _ptr(yp), rows_capacity, _ptr(ws), ws.numel() * ws.element_size(),
           _stream(stream))
 
 
@@ -175,10 +181,10 @@ def moe_unpermute_combine(yp, slot_to_row, topk_w, T, k, d, y, stream=None):
           _stream(stream))
 
 
-def moe_forward(T, d, E, k, I, pad_m, x, logits, w13, w13_sf, w2, w2_sf, y, ws,
+def moe_forward(T, d, E, k, I, kernel, x, logits, w13, w13_sf, w2, w2_sf, y, ws,
                 topk_ids_out=None, topk_w_out=None, stream=None):
     W = _Weights(_ptr(w13), _ptr(w13_sf), _ptr(w2), _ptr(w2_sf))
-    _call("moe_forward", ctypes.byref(_Dims(T, d, E, k, I)), pad_m, _ptr(x), _ptr(logits),
+    _call("moe_forward", ctypes.byref(_Dims(T, d, E, k, I)), kernel, _ptr(x), _ptr(logits),
           ctypes.byref(W), _ptr(y), _ptr(topk_ids_out), _ptr(topk_w_out), _ptr(ws),
           ws.numel() * ws.element_size(), _stream(stream))
 

@@ -10,7 +10,17 @@ using moe::tiled_sf_offset;
 
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
-constexpr int kGemmPad = 128;
+constexpr int kGroupPad = 128;  // grouped rows: every expert's group is a multiple of 128
+
+bool kernel_ok(int32_t kernel) {
+  return kernel == MOE_GEMM_TOKEN_TILES || kernel == MOE_GEMM_WEIGHT_TILES;
+}
+
+// The grouped-GEMM kernels moe_forward uses for MOE_GEMM_AUTO: weight tiles
+// while an expert gets fewer than 64 tokens on average, token tiles beyond.
+int32_t auto_kernel(int32_t T, int32_t E, int32_t k) {
+  return int64_t(T) * k < int64_t(64) * E ? MOE_GEMM_WEIGHT_TILES : MOE_GEMM_TOKEN_TILES;
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -51,7 +61,8 @@ struct ForwardLayout {
   int64_t rows_cap;
 };
 
-ForwardLayout forward_layout(const moe_dims& D, int32_t pad_m) {
+ForwardLayout forward_layout(const moe_dims& D) {
+  const int32_t pad_m = kGroupPad;
   ForwardLayout L{};
   const size_t slots = size_t(D.T) * size_t(D.k);
   L.rows_cap = rows_capacity_of(D.T, D.E, D.k, pad_m);
@@ -87,22 +98,24 @@ moe_status check_dims(const moe_dims* D) {
   return check_width(D->I);
 }
 
-moe_status check_gemm_args(int32_t E, int32_t K, int32_t N, int32_t pad_m, int64_t rows_capacity,
-                           const void* a, const void* a_sf, const int32_t* offsets,
+moe_status check_gemm_args(int32_t E, int32_t K, int32_t N, int32_t kernel, int64_t rows_capacity,
+                           const void* a, const void* a_sf, const int32_t* counts,
+                           const int32_t* offsets,
                            const void* b, const void* b_sf, const void* out, const void* out_sf,
                            bool need_out_sf, const void* ws, size_t ws_bytes) {
-  if (!a || !a_sf || !offsets || !b || !b_sf || !out || !ws || (need_out_sf && !out_sf))
+  if (!a || !a_sf || !counts || !offsets || !b || !b_sf || !out || !ws ||
+      (need_out_sf && !out_sf))
     return MOE_ERR_INVALID_ARGUMENT;
   if (E < 0 || rows_capacity < 0) return MOE_ERR_INVALID_ARGUMENT;
   if (E < 1 || E > kMaxE) return MOE_ERR_UNSUPPORTED;
   moe_status s;
   if ((s = check_width(K)) != MOE_OK) return s;
   if ((s = check_width(N)) != MOE_OK) return s;
-  if (pad_m != kGemmPad) return MOE_ERR_UNSUPPORTED;
+  if (!kernel_ok(kernel)) return MOE_ERR_UNSUPPORTED;
   if (rows_capacity % 128 != 0 || rows_capacity >= int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
   if (!aligned(a, 16) || !aligned(a_sf, 16) || !aligned(b, 32) || !aligned(b_sf, 16) ||
       !aligned(out, 16) || (need_out_sf && !aligned(out_sf, 4)) || !aligned(offsets, 4) ||
-      !aligned(ws, 4))
+      !aligned(counts, 4) || !aligned(ws, 4))
     return MOE_ERR_INVALID_ARGUMENT;
   if (ws_bytes < MOE_STATUS_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return MOE_OK;
@@ -135,6 +148,11 @@ int32_t moe_abi_version(void) { return 1; }
 size_t moe_tiled_scale_bytes(int64_t rows, int32_t K) {
   if (rows < 0 || check_width(K) != MOE_OK) return 0;
   return tiled_bytes(rows, K);
+}
+
+int32_t moe_default_kernel(int32_t T, int32_t E, int32_t k) {
+  if (check_routing_shape(T, E, k) != MOE_OK) return -1;
+  return auto_kernel(T, E, k);
 }
 
 int64_t moe_rows_capacity(int32_t T, int32_t E, int32_t k, int32_t pad_m) {
@@ -186,7 +204,7 @@ moe_status moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k,
     return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (ws_bytes < moe_permute_workspace_size(T, E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return from_cuda(moe::launch_permute(topk_ids, T, E, k, pad_m, counts, offsets, slot_to_row,
-                                       row_to_slot, at<int>(ws, MOE_STATUS_BYTES),
+                                       row_to_slot, rows_capacity, at<int>(ws, MOE_STATUS_BYTES),
                                        static_cast<int*>(ws), stream));
 }
 
@@ -207,30 +225,37 @@ moe_status moe_quant_mxfp8(const uint16_t* x, int32_t T, int32_t d, const int32_
   return from_cuda(moe::launch_quant_mxfp8(x, T, d, slot_to_row, k, codes, scales, stream));
 }
 
-moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int32_t* offsets,
-                                    int32_t E, int32_t d, int32_t I, int32_t pad_m,
-                                    const uint8_t* w13, const uint8_t* w13_sf, uint8_t* hq,
-                                    uint8_t* hs, int64_t rows_capacity, void* ws,
+moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int32_t* counts,
+                                    const int32_t* offsets, int32_t E, int32_t d, int32_t I,
+                                    int32_t kernel, const uint8_t* w13, const uint8_t* w13_sf,
+                                    uint8_t* hq, uint8_t* hs, int64_t rows_capacity, void* ws,
                                     size_t ws_bytes, cudaStream_t stream) {
-  moe_status s = check_gemm_args(E, d, I, pad_m, rows_capacity, xq, xs, offsets, w13, w13_sf, hq,
-                                 hs, true, ws, ws_bytes);
+  moe_status s = check_gemm_args(E, d, I, kernel, rows_capacity, xq, xs, counts, offsets, w13,
+                                 w13_sf, hq, hs, true, ws, ws_bytes);
   if (s != MOE_OK) return s;
   if (rows_capacity == 0) return MOE_OK;
-  return from_cuda(moe::launch_gemm_w13_glu(xq, xs, offsets, E, d, I, w13, w13_sf, hq, hs,
-                                            rows_capacity, static_cast<int*>(ws), stream));
+  if (kernel == MOE_GEMM_WEIGHT_TILES)
+    return from_cuda(moe::launch_gemm_decode_w13_glu(xq, xs, counts, offsets, E, d, I, w13,
+                                                     w13_sf, hq, hs, rows_capacity,
+                                                     static_cast<int*>(ws), stream));
+  return from_cuda(moe::launch_gemm_w13_glu(xq, xs, counts, offsets, E, d, I, w13, w13_sf, hq,
+                                            hs, rows_capacity, static_cast<int*>(ws), stream));
 }
 
-moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32_t* offsets,
-                               int32_t E, int32_t I, int32_t d, int32_t pad_m,
-                               const uint8_t* w2, const uint8_t* w2_sf, uint16_t* yp,
-                               int64_t rows_capacity, void* ws, size_t ws_bytes,
+moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32_t* counts,
+                               const int32_t* offsets, int32_t E, int32_t I, int32_t d,
+                               int32_t kernel, const uint8_t* w2, const uint8_t* w2_sf,
+                               uint16_t* yp, int64_t rows_capacity, void* ws, size_t ws_bytes,
                                cudaStream_t stream) {
-  moe_status s = check_gemm_args(E, I, d, pad_m, rows_capacity, hq, hs, offsets, w2, w2_sf, yp,
-                                 nullptr, false, ws, ws_bytes);
+  moe_status s = check_gemm_args(E, I, d, kernel, rows_capacity, hq, hs, counts, offsets, w2,
+                                 w2_sf, yp, nullptr, false, ws, ws_bytes);
   if (s != MOE_OK) return s;
   if (rows_capacity == 0) return MOE_OK;
-  return from_cuda(moe::launch_gemm_w2(hq, hs, offsets, E, I, d, w2, w2_sf, yp, rows_capacity,
-                                       static_cast<int*>(ws), stream));
+  if (kernel == MOE_GEMM_WEIGHT_TILES)
+    return from_cuda(moe::launch_gemm_decode_w2(hq, hs, counts, offsets, E, I, d, w2, w2_sf, yp,
+                                                rows_capacity, static_cast<int*>(ws), stream));
+  return from_cuda(moe::launch_gemm_w2(hq, hs, counts, offsets, E, I, d, w2, w2_sf, yp,
+                                       rows_capacity, static_cast<int*>(ws), stream));
 }
 
 moe_status moe_unpermute_combine(const uint16_t* yp, const int32_t* slot_to_row,
@@ -248,22 +273,23 @@ moe_status moe_unpermute_combine(const uint16_t* yp, const int32_t* slot_to_row,
   return from_cuda(moe::launch_combine(yp, slot_to_row, topk_w, T, k, d, y, stream));
 }
 
-moe_status moe_workspace_size(const moe_dims* dims, int32_t pad_m, size_t* bytes) {
+moe_status moe_workspace_size(const moe_dims* dims, size_t* bytes) {
   if (!bytes) return MOE_ERR_INVALID_ARGUMENT;
   moe_status s = check_dims(dims);
   if (s != MOE_OK) return s;
-  if (pad_m != kGemmPad) return MOE_ERR_UNSUPPORTED;
-  *bytes = forward_layout(*dims, pad_m).total;
+  *bytes = forward_layout(*dims).total;
   return MOE_OK;
 }
 
-moe_status moe_forward(const moe_dims* dims, int32_t pad_m, const uint16_t* x,
+moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
                        const float* logits, const moe_weights* W, uint16_t* y,
                        int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
                        cudaStream_t stream) {
   moe_status s = check_dims(dims);
   if (s != MOE_OK) return s;
-  if (pad_m != kGemmPad) return MOE_ERR_UNSUPPORTED;
+  if (kernel == MOE_GEMM_AUTO) kernel = auto_kernel(dims->T, dims->E, dims->k);
+  if (!kernel_ok(kernel)) return MOE_ERR_UNSUPPORTED;
+  const int32_t pad_m = kGroupPad;
   const moe_dims D = *dims;
   if (D.T == 0) return MOE_OK;
   if (!x || !logits || !W || !y || !ws || !W->w13 || !W->w13_sf || !W->w2 || !W->w2_sf)
@@ -273,7 +299,7 @@ moe_status moe_forward(const moe_dims* dims, int32_t pad_m, const uint16_t* x,
       !aligned(W->w2_sf, 16) || (topk_ids_out && !aligned(topk_ids_out, 4)) ||
       (topk_w_out && !aligned(topk_w_out, 4)))
     return MOE_ERR_INVALID_ARGUMENT;
-  const ForwardLayout L = forward_layout(D, pad_m);
+  const ForwardLayout L = forward_layout(D);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
 
   int* status = at<int>(ws, L.status);
@@ -295,17 +321,27 @@ moe_status moe_forward(const moe_dims* dims, int32_t pad_m, const uint16_t* x,
 
   if ((e = moe::launch_route_topk(logits, D.T, D.E, D.k, ids, w, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if ((e = moe::launch_permute(ids, D.T, D.E, D.k, pad_m, counts, offsets, s2r, r2s,
+  if ((e = moe::launch_permute(ids, D.T, D.E, D.k, pad_m, counts, offsets, s2r, r2s, L.rows_cap,
                                at<int>(ws, L.hist), status, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   if ((e = moe::launch_quant_mxfp8(x, D.T, D.d, s2r, D.k, xq, xs, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if ((e = moe::launch_gemm_w13_glu(xq, xs, offsets, D.E, D.d, D.I, W->w13, W->w13_sf, hq, hs,
-                                    L.rows_cap, status, stream)) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if ((e = moe::launch_gemm_w2(hq, hs, offsets, D.E, D.I, D.d, W->w2, W->w2_sf, yp, L.rows_cap,
-                               status, stream)) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (kernel == MOE_GEMM_WEIGHT_TILES) {
+    if ((e = moe::launch_gemm_decode_w13_glu(xq, xs, counts, offsets, D.E, D.d, D.I, W->w13,
+                                             W->w13_sf, hq, hs, L.rows_cap, status, stream)) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    if ((e = moe::launch_gemm_decode_w2(hq, hs, counts, offsets, D.E, D.I, D.d, W->w2, W->w2_sf,
+                                        yp, L.rows_cap, status, stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else {
+    if ((e = moe::launch_gemm_w13_glu(xq, xs, counts, offsets, D.E, D.d, D.I, W->w13, W->w13_sf,
+                                      hq, hs, L.rows_cap, status, stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if ((e = moe::launch_gemm_w2(hq, hs, counts, offsets, D.E, D.I, D.d, W->w2, W->w2_sf, yp,
+                                 L.rows_cap, status, stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   return from_cuda(moe::launch_combine(yp, s2r, w, D.T, D.k, D.d, y, stream));
 }
 

@@ -14,15 +14,17 @@
 // scale per 32 inputs on each side, via tcgen05.mma kind::mxf8f6f4
 // (4 MMAs of K = 32 per stage, fp32 accumulators in tensor memory).
 //
-// CTA organisation (persistent, one CTA per SM, 192 threads):
+// CTA organisation (persistent, one CTA per SM, 320 threads):
 //   warp 0      TMA producer: A box 128x128 bytes, B box(es) of E2M1 expanded
 //               by TMA to one byte slot per element (16U4_ALIGN16B), both
 //               128-byte swizzled; the stage's scale atoms by bulk copy.
 //   warp 1      tensor-memory allocator + single-thread MMA issuer: copies the
 //               stage's scale atoms into tensor memory (tcgen05.cp), issues
 //               the 4 MMAs, frees the smem stage with tcgen05.commit.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one row per thread),
-//               fused GLU + MX requant (MODE 0) or bf16 conversion (MODE 1).
+//   warps 2-9   epilogue: tcgen05.ld of the accumulator (one row and half the
+//               columns per thread) straight into registers, release of the
+//               accumulator, then the fused GLU + MX requant (MODE 0) or the
+//               bf16 conversion (MODE 1) overlapped with the next tile's MMAs.
 // Tiles are (expert, n-tile, m-tile) with the m-tile fastest, so CTAs running
 // at the same time share one expert's weight tile through L2. The expert row
 // offsets are read on the device: no host synchronisation.
@@ -39,7 +41,7 @@ constexpr int BM = 128;            // rows per tile (MMA M)
 constexpr int BK = 128;            // inputs per pipeline stage
 constexpr int BN = 256;            // MMA N
 constexpr int STAGES = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, 256)
 constexpr uint32_t kSfCol = 256;   // scale slots: 16 columns per stage (A: 4, B: 8)
@@ -63,11 +65,13 @@ constexpr uint32_t kNumBars = 2 * STAGES + 3;  // full[S], empty[S], acc_full, a
 constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
 constexpr uint32_t kOffSched = kOffMisc + 16;
 constexpr uint32_t kMaxE = 1024;
-constexpr uint32_t kSmemBytes = kOffSched + 2 * (kMaxE + 1) * 4 + 1024;
+constexpr uint32_t kSmemBytes = kOffSched + 3 * (kMaxE + 1) * 4 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct GemmParams {
   const uint8_t* a_sf;   // TILED scales of A
   const uint8_t* b_sf;   // TILED scales of B
+  const int* counts;     // [E] tokens per expert
   const int* offsets;    // [E+1]
   int E;
   int K;                 // inputs per row (d for MODE 0, I for MODE 1)
@@ -81,8 +85,10 @@ struct GemmParams {
   int* status;
 };
 
-__device__ __forceinline__ void decode_tile(int tile, const int* prefix, const int* offs, int E,
-                                            int& e, int& nt, int& row0) {
+// Tile -> (expert, n-tile, first row). An expert's m-tiles cover its tokens
+// (ceil(counts[e]/BM) of them); the m-tile index runs fastest.
+__device__ __forceinline__ void decode_tile(int tile, const int* prefix, const int* offs,
+                                            const int* cnts, int E, int& e, int& nt, int& row0) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -91,7 +97,7 @@ __device__ __forceinline__ void decode_tile(int tile, const int* prefix, const i
   }
   e = lo;
   const int r = tile - prefix[e];
-  const int mtiles = (offs[e + 1] - offs[e]) / BM;
+  const int mtiles = (cnts[e] + BM - 1) / BM;
   nt = r / mtiles;
   row0 = offs[e] + (r - nt * mtiles) * BM;
 }
@@ -113,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* total_holder = reinterpret_cast<int*>(smem + kOffMisc + 8);
   int* prefix = reinterpret_cast<int*>(smem + kOffSched);
   int* offs = prefix + (kMaxE + 1);
+  int* cnts = offs + (kMaxE + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
@@ -124,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4 * 32);
+    mbar_init(acc_empty, 8 * 32);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -133,17 +140,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
-  for (int i = threadIdx.x; i <= E; i += kThreads) offs[i] = p.offsets[i];
+  for (int i = threadIdx.x; i <= E; i += kThreads) {
+    offs[i] = p.offsets[i];
+    if (i < E) cnts[i] = p.counts[i];
+  }
   __syncthreads();
   if (warp == 0) {  // tile prefix over experts: lane owns a run of experts
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
     int s = 0;
-    bool bad = false;  // every group must be a non-negative multiple of BM rows
+    bool bad = false;  // groups must be multiples of BM rows holding their counts
     for (int e = e0; e < e1; ++e) {
       const int rows = offs[e + 1] - offs[e];
-      bad |= rows < 0 || rows % BM != 0;
-      s += max(0, rows / BM) * p.n_tiles;
+      bad |= rows < 0 || rows % BM != 0 || cnts[e] < 0 || cnts[e] > rows;
+      s += max(0, (cnts[e] + BM - 1) / BM) * p.n_tiles;
     }
     bad = __any_sync(0xffffffffu, bad);
     int incl = s;
@@ -155,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = incl - s;
     for (int e = e0; e < e1; ++e) {
       prefix[e] = run;
-      run += max(0, (offs[e + 1] - offs[e]) / BM) * p.n_tiles;
+      run += max(0, (cnts[e] + BM - 1) / BM) * p.n_tiles;
     }
     if (lane == 31) {
       const bool ok = !bad && offs[0] == 0 && int64_t(offs[E]) <= p.rows_capacity;
@@ -177,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t filled = 0, last_parity = 0;  // per-stage bits of the last fill
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
         int e, nt, row0;
-        decode_tile(tile, prefix, offs, E, e, nt, row0);
+        decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
         bool failed = false;
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -288,11 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // the tensor-memory lane quarter this warp may access
+    // Eight warps, two per tensor-memory lane quarter (a warp may only access
+    // quarter warp%4); the two split the tile's columns in halves. A warp
+    // copies its 32 rows x 128 accumulator columns into registers, hands the
+    // accumulator back to the MMA issuer at once, and finishes the math and
+    // the stores while the next tile accumulates.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, nt, row0;
-      decode_tile(tile, prefix, offs, E, e, nt, row0);
+      decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
       bool ok = mbar_wait(acc_full, acc_phase, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -303,64 +319,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t row = int64_t(row0) + q * 32 + lane;
       const uint32_t tq = tmem_base + kAccCol + (uint32_t(q * 32) << 16);
+      // MODE 0: gate columns [64 half, 64 half + 64) and the matching up
+      // columns (+128). MODE 1: output columns [128 half, 128 half + 128).
+      const bool active = MODE == 0 || nt * BN + half * 128 < p.d;
+      uint32_t v[4][32];
+      if (MODE == 0) {
+        tmem_ld_32x32b_x32(tq + 64 * half, v[0]);
+        tmem_ld_32x32b_x32(tq + 64 * half + 32, v[1]);
+        tmem_ld_32x32b_x32(tq + 128 + 64 * half, v[2]);
+        tmem_ld_32x32b_x32(tq + 128 + 64 * half + 32, v[3]);
+      } else if (active) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tq + 128 * half + 32 * c, v[c]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      acc_phase ^= 1u;
       if (MODE == 0) {
         uint32_t sword = 0;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld_32x32b_x32(tq + c * 32, g);
-          tmem_ld_32x32b_x32(tq + 128 + c * 32, u);
-          tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
           float h[32];
           float amax = 0.0f;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float gf = __uint_as_float(g[i]);
-            const float uf = __uint_as_float(u[i]);
-            h[i] = gf / (1.0f + expf(-gf)) * uf;
+            const float gf = __uint_as_float(v[c][i]);
+            const float uf = __uint_as_float(v[2 + c][i]);
+            h[i] = __fdividef(gf * uf, 1.0f + __expf(-gf));  // silu(g) * u
             amax = fmaxf(amax, fabsf(h[i]));
           }
           const int code = mx_scale_code(amax);
           const float m = mx_scale_mult(code);
           uint4 o[2];
 #pragma unroll
-          for (int v = 0; v < 2; ++v) {
-            o[v].x = e4m3x4(h[16 * v + 0], h[16 * v + 1], h[16 * v + 2], h[16 * v + 3], m);
-            o[v].y = e4m3x4(h[16 * v + 4], h[16 * v + 5], h[16 * v + 6], h[16 * v + 7], m);
-            o[v].z = e4m3x4(h[16 * v + 8], h[16 * v + 9], h[16 * v + 10], h[16 * v + 11], m);
-            o[v].w = e4m3x4(h[16 * v + 12], h[16 * v + 13], h[16 * v + 14], h[16 * v + 15], m);
+          for (int w = 0; w < 2; ++w) {
+            o[w].x = e4m3x4(h[16 * w + 0], h[16 * w + 1], h[16 * w + 2], h[16 * w + 3], m);
+            o[w].y = e4m3x4(h[16 * w + 4], h[16 * w + 5], h[16 * w + 6], h[16 * w + 7], m);
+            o[w].z = e4m3x4(h[16 * w + 8], h[16 * w + 9], h[16 * w + 10], h[16 * w + 11], m);
+            o[w].w = e4m3x4(h[16 * w + 12], h[16 * w + 13], h[16 * w + 14], h[16 * w + 15], m);
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.out_q + row * p.I + int64_t(nt) * 128 + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(p.out_q + row * p.I + int64_t(nt) * 128 +
+                                                (2 * half + c) * 32);
           dst[0] = o[0];
           dst[1] = o[1];
           sword |= uint32_t(code) << (8 * c);
         }
-        *reinterpret_cast<uint32_t*>(p.out_sf + tiled_sf_offset(row, int64_t(nt) * 4, p.I)) =
-            sword;
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          const int col = nt * BN + c * 32;
-          if (col >= p.d) break;  // warp-uniform
-          uint32_t a[32];
-          tmem_ld_32x32b_x32(tq + c * 32, a);
-          tmem_ld_wait();
+        *reinterpret_cast<uint16_t*>(
+            p.out_sf + tiled_sf_offset(row, int64_t(nt) * 4 + 2 * half, p.I)) = uint16_t(sword);
+      } else if (active) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
           uint32_t o[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const __nv_bfloat162 b2 =
-                __floats2bfloat162_rn(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[c][2 * i]),
+                                                            __uint_as_float(v[c][2 * i + 1]));
             o[i] = *reinterpret_cast<const uint32_t*>(&b2);
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + row * p.d + col);
+          uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + row * p.d + nt * BN + 128 * half +
+                                                32 * c);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          for (int w = 0; w < 4; ++w)
+            dst[w] = make_uint4(o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(acc_empty);
-      acc_phase ^= 1u;
     }
   }
 
@@ -383,6 +406,23 @@ __global__ void wait_timeout_selftest_kernel(int* status, uint64_t limit_ns) {
     if (!mbar_wait(&bar, 0, nullptr, limit_ns)) set_status(status, MOE_ERR_DEVICE_TIMEOUT);
   }
 }
+
+template <int MODE>
+cudaError_t launch_mode(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                        cudaStream_t st) {
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+  if (err != cudaSuccess) return err;
+  const int64_t max_tiles = (p.rows_capacity / BM) * p.n_tiles;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = int(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
+  grouped_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -410,7 +450,7 @@ bool encode_operand(CUtensorMap* map, const void* base, bool e2m1, int K, int64_
   if (!fn) return false;
   const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
   const cuuint64_t strides[1] = {cuuint64_t(e2m1 ? K / 2 : K)};
-  const cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
+  const cuuint32_t box[2] = {128u, cuuint32_t(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r =
       fn(map, e2m1 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
@@ -427,33 +467,17 @@ int sm_count() {
   return n;
 }
 
-template <int MODE>
-cudaError_t launch_mode(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                        cudaStream_t st) {
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kSmemBytes));
-  if (err != cudaSuccess) return err;
-  const int64_t max_tiles = (p.rows_capacity / BM) * p.n_tiles;
-  const int sms = sm_count();
-  if (sms <= 0) return cudaErrorInvalidDevice;
-  const int grid = int(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
-  grouped_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(ta, tb, p);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
-cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* offsets, int E,
-                                int d, int I, const uint8_t* w13, const uint8_t* w13_sf,
-                                uint8_t* hq, uint8_t* hs, int64_t rows_capacity, int* status,
-                                cudaStream_t st) {
+cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,
+                                const int* offsets, int E, int d, int I, const uint8_t* w13,
+                                const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
+                                int64_t rows_capacity, int* status, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!encode_operand(&ta, xq, false, d, rows_capacity, BM)) return cudaErrorInvalidValue;
   if (!encode_operand(&tb, w13, true, d, int64_t(E) * 2 * I, 128)) return cudaErrorInvalidValue;
   GemmParams p{};
   p.a_sf = xs;
   p.b_sf = w13_sf;
+  p.counts = counts;
   p.offsets = offsets;
   p.E = E;
   p.K = d;
@@ -467,15 +491,17 @@ cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int*
   return launch_mode<0>(p, ta, tb, st);
 }
 
-cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* offsets, int E, int I,
-                           int d, const uint8_t* w2, const uint8_t* w2_sf, uint16_t* yp,
-                           int64_t rows_capacity, int* status, cudaStream_t st) {
+cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* counts,
+                           const int* offsets, int E, int I, int d, const uint8_t* w2,
+                           const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity, int* status,
+                           cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!encode_operand(&ta, hq, false, I, rows_capacity, BM)) return cudaErrorInvalidValue;
   if (!encode_operand(&tb, w2, true, I, int64_t(E) * d, BN)) return cudaErrorInvalidValue;
   GemmParams p{};
   p.a_sf = hs;
   p.b_sf = w2_sf;
+  p.counts = counts;
   p.offsets = offsets;
   p.E = E;
   p.K = I;

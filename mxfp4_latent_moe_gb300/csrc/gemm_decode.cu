@@ -1,0 +1,428 @@
+// Grouped GEMMs of the routed experts for few tokens per expert (decode
+// batches), on tcgen05 block-scaled tensor cores with the operands swapped:
+// the expert's weights are the MMA's M side (128 weight rows per MMA) and its
+// tokens the N side, so an expert holding a handful of tokens costs N = 32 of
+// tensor work (not M = 128) while its weights stream from HBM exactly once.
+//
+// Same layer steps as gemm.cu ("The MXFP4 latent MoE on FlyDSL" of "Kimi K3.1
+// Pro on AMD Instinct GPUs"; Experts row of "Kimi K3.1 Pro at a glance"):
+//   stage 1 (MODE 0): G = W1 . Xq^T and U = W3 . Xq^T, two MMAs per K step into
+//                     two accumulators that share tensor-memory lanes, then
+//                     h = silu(G) * U -> MXFP8 in the epilogue
+//   stage 2 (MODE 1): Yp^T = W2 . Hq^T for 256 output features per tile (two
+//                     MMAs of 128 weight rows), -> bf16
+// MXFP4 weights are the A operand (E2M1, kind::mxf8f6f4 format 5), MXFP8
+// activations the B operand (E4M3), one E8M0 scale per 32 inputs each side.
+//
+// Groups are padded to 128 rows (as for gemm.cu) and the per-expert token
+// counts are read on the device: a tile is (expert, weight rows, 128-row chunk
+// of the group) with N = the chunk's tokens rounded up to 32. Every token
+// chunk starts on a 128-row scale atom, so the tokens' scales go to tensor
+// memory with one aligned copy per stage; padding rows past N are never read.
+//
+// CTA: persistent, one per SM, 320 threads: warp 0 TMA producer, warp 1
+// tensor-memory allocator + single-thread MMA issuer, warps 2-9 epilogue (two
+// per lane quarter, each taking half the tile's tokens); the epilogue copies
+// its accumulator columns to registers and releases tensor memory before the
+// math, so the next tile's MMAs overlap it. The MX block of h is 32
+// consecutive features = the 32 lanes of one warp: its amax is one warp
+// reduction per token.
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int WM = 128;            // weight rows per MMA (M)
+constexpr int BK = 128;            // inputs per stage
+constexpr int NMAX = 128;          // tokens per tile at most
+constexpr int STAGES = 4;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAcc1Col = 128;  // second accumulator (up rows / upper w2 rows)
+constexpr uint32_t kSfCol = 256;    // scale slots: 16 columns per stage (A0, A1, B)
+
+constexpr uint32_t A_TILE = WM * BK;         // one 128-row E2M1 tile in smem (expanded)
+constexpr uint32_t A_TILE_TX = A_TILE / 2;   // its packed bytes (TMA transaction count)
+constexpr uint32_t A_STAGE = 2 * A_TILE;
+constexpr uint32_t B_BOX_ROWS = 32;
+constexpr uint32_t B_BOX = B_BOX_ROWS * BK;  // 4 KB of E4M3 tokens
+constexpr uint32_t B_STAGE = NMAX * BK;
+constexpr uint32_t SF_ATOM = 512;
+
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + STAGES * A_STAGE;
+constexpr uint32_t kOffSfa = kOffB + STAGES * B_STAGE;
+constexpr uint32_t kOffSfb = kOffSfa + STAGES * 2 * SF_ATOM;
+constexpr uint32_t kOffBars = kOffSfb + STAGES * SF_ATOM;
+constexpr uint32_t kNumBars = 2 * STAGES + 3;  // full[S], empty[S], acc_full, acc_empty, drain
+constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
+constexpr uint32_t kOffSched = kOffMisc + 16;
+constexpr uint32_t kMaxE = 1024;
+constexpr uint32_t kSmemBytes = kOffSched + 3 * (kMaxE + 1) * 4 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct DecodeParams {
+  const uint8_t* a_sf;  // TILED scales of the weights
+  const uint8_t* b_sf;  // TILED scales of the activations
+  const int* counts;    // [E] tokens per expert
+  const int* offsets;   // [E+1] group offsets (multiples of 128)
+  int E;
+  int K;                // inputs per row
+  int I;                // MODE 0: h width; MODE 1: w2 inputs
+  int d;                // MODE 1: output width
+  int n_tiles;          // weight tiles per expert: I/128 (MODE 0), ceil(d/256) (MODE 1)
+  int64_t rows_capacity;
+  uint8_t* out_q;       // MODE 0: hq [rows][I]
+  uint8_t* out_sf;      // MODE 0: hs TILED (rows, I)
+  uint16_t* out_bf16;   // MODE 1: yp [rows][d]
+  int* status;
+};
+
+__device__ __forceinline__ void decode_tile(int tile, const int* prefix, const int* offs,
+                                            const int* cnts, int E, int& e, int& nt, int& row0,
+                                            int& ntok) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  e = lo;
+  const int cnt = cnts[e];
+  const int chunks = (cnt + NMAX - 1) / NMAX;
+  const int r = tile - prefix[e];
+  nt = r / chunks;
+  const int ch = r - nt * chunks;
+  row0 = offs[e] + ch * NMAX;
+  ntok = (min(NMAX, cnt - ch * NMAX) + 31) & ~31;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                               const __grid_constant__ CUtensorMap tmap_x, const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* total_holder = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  int* prefix = reinterpret_cast<int*>(smem + kOffSched);
+  int* offs = prefix + (kMaxE + 1);
+  int* cnts = offs + (kMaxE + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  const int KT = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 8 * 32);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i <= E; i += kThreads) {
+    offs[i] = p.offsets[i];
+    if (i < E) cnts[i] = p.counts[i];
+  }
+  __syncthreads();
+  if (warp == 0) {  // tile prefix over experts: lane owns a run of experts
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int s = 0;
+    bool bad = false;  // groups must be multiples of 128 rows holding their counts
+    for (int e = e0; e < e1; ++e) {
+      const int rows = offs[e + 1] - offs[e];
+      bad |= rows < 0 || rows % NMAX != 0 || cnts[e] < 0 || cnts[e] > rows;
+      s += max(0, (cnts[e] + NMAX - 1) / NMAX) * p.n_tiles;
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    int incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += n;
+    }
+    int run = incl - s;
+    for (int e = e0; e < e1; ++e) {
+      prefix[e] = run;
+      run += max(0, (cnts[e] + NMAX - 1) / NMAX) * p.n_tiles;
+    }
+    if (lane == 31) {
+      const bool ok = !bad && offs[0] == 0 && int64_t(offs[E]) <= p.rows_capacity;
+      if (!ok && blockIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE_BAD_INPUT);
+      prefix[E] = incl;
+      *total_holder = ok ? incl : 0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = *total_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t filled = 0, last_parity = 0;
+      bool failed = false;
+      for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
+        int e, nt, row0, ntok;
+        decode_tile(tile, prefix, offs, cnts, E, e, nt, row0, ntok);
+        // weight rows: MODE 0 gate and up rows, MODE 1 the tile's two 128-row halves
+        const int64_t wrow0 = MODE == 0 ? int64_t(e) * 2 * p.I + int64_t(nt) * WM
+                                        : int64_t(e) * p.d + int64_t(nt) * 2 * WM;
+        const bool two = MODE == 0 || nt * 2 * WM + WM < p.d;
+        const int64_t wrow1 = MODE == 0 ? wrow0 + p.I : wrow0 + WM;
+        const uint32_t tx = (two ? 2u : 1u) * (A_TILE_TX + SF_ATOM) +
+                            uint32_t(ntok / int(B_BOX_ROWS)) * B_BOX + SF_ATOM;
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            failed = true;
+            break;
+          }
+          uint8_t* sa = smem + kOffA + stage * A_STAGE;
+          uint8_t* sb = smem + kOffB + stage * B_STAGE;
+          uint8_t* ssfa = smem + kOffSfa + stage * 2 * SF_ATOM;
+          uint8_t* ssfb = smem + kOffSfb + stage * SF_ATOM;
+          mbar_arrive_expect_tx(&full[stage], tx);
+          tma_load_2d(sa, &tmap_w, &full[stage], kt * BK, int(wrow0));
+          bulk_load(ssfa, p.a_sf + ((wrow0 >> 7) * KT + kt) * SF_ATOM, SF_ATOM, &full[stage]);
+          if (two) {
+            tma_load_2d(sa + A_TILE, &tmap_w, &full[stage], kt * BK, int(wrow1));
+            bulk_load(ssfa + SF_ATOM, p.a_sf + ((wrow1 >> 7) * KT + kt) * SF_ATOM, SF_ATOM,
+                      &full[stage]);
+          }
+          for (int j = 0; j < ntok / int(B_BOX_ROWS); ++j)
+            tma_load_2d(sb + j * B_BOX, &tmap_x, &full[stage], kt * BK, row0 + j * B_BOX_ROWS);
+          bulk_load(ssfb, p.b_sf + (int64_t(row0 >> 7) * KT + kt) * SF_ATOM, SF_ATOM,
+                    &full[stage]);
+          filled |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if ((filled >> s) & 1u)
+          if (!mbar_wait(&full[s], (last_parity >> s) & 1u, nullptr))
+            set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      bool failed = false;
+      for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
+        int e, nt, row0, ntok;
+        decode_tile(tile, prefix, offs, cnts, E, e, nt, row0, ntok);
+        const bool two = MODE == 0 || nt * 2 * WM + WM < p.d;
+        const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, WM, ntok);
+        if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + kOffA + stage * A_STAGE);
+          const uint32_t sb = smem_u32(smem + kOffB + stage * B_STAGE);
+          const uint32_t ssfa = smem_u32(smem + kOffSfa + stage * 2 * SF_ATOM);
+          const uint32_t ssfb = smem_u32(smem + kOffSfb + stage * SF_ATOM);
+          const uint32_t sf_t = tmem_base + kSfCol + stage * 16;  // A0: +0, A1: +4, B: +8
+          tc_cp_32x128b_x4(sf_t, desc_sf_block(ssfa));
+          if (two) tc_cp_32x128b_x4(sf_t + 4, desc_sf_block(ssfa + SF_ATOM));
+          tc_cp_32x128b_x4(sf_t + 8, desc_sf_block(ssfb));
+          const uint64_t adesc = desc_sw128_kmajor(sa);
+          const uint64_t bdesc = desc_sw128_kmajor(sb);
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint32_t id = idesc_with_sf_id(idesc, uint32_t(kk));
+            const uint32_t accum = (kt > 0 || kk > 0) ? 1u : 0u;
+            tc_mma_mx(tmem_base, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), id, sf_t,
+                      sf_t + 8, accum);
+            if (two)
+              tc_mma_mx(tmem_base + kAcc1Col, adesc + uint64_t((A_TILE >> 4) + 2 * kk),
+                        bdesc + uint64_t(2 * kk), id, sf_t + 4, sf_t + 8, accum);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (failed) break;
+        tc_commit(acc_full);
+        acc_phase ^= 1u;
+      }
+      if (failed) {
+        *abort_flag = 1;
+        set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+      }
+      tc_commit(drain);
+      if (!mbar_wait(drain, 0, nullptr)) set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // Thread = one weight row (tensor-memory lane) of the tile; the two warps
+    // of a lane quarter split the tile's tokens in halves of ntok/2 (16..64).
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, nt, row0, ntok;
+      decode_tile(tile, prefix, offs, cnts, E, e, nt, row0, ntok);
+      const bool two = MODE == 0 || nt * 2 * WM + WM < p.d;
+      bool ok = mbar_wait(acc_full, acc_phase, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const int hn = ntok >> 1;          // tokens of this warp
+      const int t0 = half * hn;          // first of them
+      const int nch = hn >> 4;           // 16-token chunks (1..4)
+      const uint32_t tq = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(t0);
+      uint32_t v0[4][16], v1[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (c < nch) {
+          tmem_ld_32x32b_x16(tq + 16 * c, v0[c]);
+          if (two) tmem_ld_32x32b_x16(tq + kAcc1Col + 16 * c, v1[c]);
+        }
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      acc_phase ^= 1u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (c >= nch) break;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int64_t row = int64_t(row0) + t0 + 16 * c + i;
+          if (MODE == 0) {
+            const float gf = __uint_as_float(v0[c][i]);
+            const float h = __fdividef(gf * __uint_as_float(v1[c][i]), 1.0f + __expf(-gf));
+            // amax over the warp's 32 features = one MX block of the token's h row
+            const float amax =
+                __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
+            const int code = mx_scale_code(amax);
+            const int feat = nt * WM + q * 32 + lane;
+            p.out_q[row * p.I + feat] = uint8_t(e4m3x2(h * mx_scale_mult(code), 0.0f) & 0xFFu);
+            if (lane == 0) p.out_sf[tiled_sf_offset(row, feat >> 5, p.I)] = uint8_t(code);
+          } else {
+            const int feat = nt * 2 * WM + q * 32 + lane;
+            p.out_bf16[row * p.d + feat] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v0[c][i])));
+            if (two)
+              p.out_bf16[row * p.d + feat + WM] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v1[c][i])));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template <int MODE>
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tw, const CUtensorMap& tx,
+                          cudaStream_t st) {
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_decode_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+  if (err != cudaSuccess) return err;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int64_t max_tiles = (p.rows_capacity / NMAX) * p.n_tiles;
+  const int grid = int(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
+  grouped_gemm_decode_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(tw, tx, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_decode_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,
+                                       const int* offsets, int E, int d, int I,
+                                       const uint8_t* w13, const uint8_t* w13_sf, uint8_t* hq,
+                                       uint8_t* hs, int64_t rows_capacity, int* status,
+                                       cudaStream_t st) {
+  CUtensorMap tw, tx;
+  if (!encode_operand(&tw, w13, true, d, int64_t(E) * 2 * I, WM)) return cudaErrorInvalidValue;
+  if (!encode_operand(&tx, xq, false, d, rows_capacity, B_BOX_ROWS)) return cudaErrorInvalidValue;
+  DecodeParams p{};
+  p.a_sf = w13_sf;
+  p.b_sf = xs;
+  p.counts = counts;
+  p.offsets = offsets;
+  p.E = E;
+  p.K = d;
+  p.I = I;
+  p.d = d;
+  p.n_tiles = I / WM;
+  p.rows_capacity = rows_capacity;
+  p.out_q = hq;
+  p.out_sf = hs;
+  p.status = status;
+  return launch_decode<0>(p, tw, tx, st);
+}
+
+cudaError_t launch_gemm_decode_w2(const uint8_t* hq, const uint8_t* hs, const int* counts,
+                                  const int* offsets, int E, int I, int d, const uint8_t* w2,
+                                  const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity,
+                                  int* status, cudaStream_t st) {
+  CUtensorMap tw, tx;
+  if (!encode_operand(&tw, w2, true, I, int64_t(E) * d, WM)) return cudaErrorInvalidValue;
+  if (!encode_operand(&tx, hq, false, I, rows_capacity, B_BOX_ROWS)) return cudaErrorInvalidValue;
+  DecodeParams p{};
+  p.a_sf = w2_sf;
+  p.b_sf = hs;
+  p.counts = counts;
+  p.offsets = offsets;
+  p.E = E;
+  p.K = I;
+  p.I = I;
+  p.d = d;
+  p.n_tiles = (d + 2 * WM - 1) / (2 * WM);
+  p.rows_capacity = rows_capacity;
+  p.out_bf16 = yp;
+  p.status = status;
+  return launch_decode<1>(p, tw, tx, st);
+}
+
+}  // namespace moe

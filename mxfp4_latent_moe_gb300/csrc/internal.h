@@ -11,21 +11,38 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int* ids
 
 size_t permute_scratch_bytes(int T, int E);
 cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* counts,
-                           int* offsets, int* slot_to_row, int* row_to_slot, int* hist,
-                           int* status, cudaStream_t st);
+                           int* offsets, int* slot_to_row, int* row_to_slot,
+                           int64_t rows_capacity, int* hist, int* status, cudaStream_t st);
 
 cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
                                uint8_t* codes, uint8_t* scales, cudaStream_t st);
 cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                                   cudaStream_t st);
 
-cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* offsets, int E,
-                                int d, int I, const uint8_t* w13, const uint8_t* w13_sf,
-                                uint8_t* hq, uint8_t* hs, int64_t rows_capacity, int* status,
-                                cudaStream_t st);
-cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* offsets, int E, int I,
-                           int d, const uint8_t* w2, const uint8_t* w2_sf, uint16_t* yp,
-                           int64_t rows_capacity, int* status, cudaStream_t st);
+cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,
+                                const int* offsets, int E, int d, int I, const uint8_t* w13,
+                                const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
+                                int64_t rows_capacity, int* status, cudaStream_t st);
+cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* counts,
+                           const int* offsets, int E, int I, int d, const uint8_t* w2,
+                           const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity, int* status,
+                           cudaStream_t st);
+// Shared by the grouped GEMMs: 2-D K-major operand tensor map (dim0 = K
+// inputs, dim1 = rows, 128-input boxes of box_rows rows, 128-byte swizzle;
+// E2M1 operands use TMA's 16U4_ALIGN16B expansion), and the SM count.
+bool encode_operand(CUtensorMap* map, const void* base, bool e2m1, int K, int64_t rows,
+                    int box_rows);
+int sm_count();
+
+cudaError_t launch_gemm_decode_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,
+                                       const int* offsets, int E, int d, int I,
+                                       const uint8_t* w13, const uint8_t* w13_sf, uint8_t* hq,
+                                       uint8_t* hs, int64_t rows_capacity, int* status,
+                                       cudaStream_t st);
+cudaError_t launch_gemm_decode_w2(const uint8_t* hq, const uint8_t* hs, const int* counts,
+                                  const int* offsets, int E, int I, int d, const uint8_t* w2,
+                                  const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity,
+                                  int* status, cudaStream_t st);
 cudaError_t launch_wait_timeout_selftest(int* status, uint32_t limit_us, cudaStream_t st);
 
 cudaError_t launch_combine(const uint16_t* yp, const int* slot_to_row, const float* w, int T,

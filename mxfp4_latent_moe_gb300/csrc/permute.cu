@@ -10,9 +10,9 @@
 // an expert at most once, so a slot's rank among the chunk's slots of its
 // expert is popc(mask of lower lanes in its warp) + popc(masks of lower warps).
 //   1. permute_count:   per-chunk expert histograms hist[c][e]
-//   2. permute_scan:    counts, padded offsets, chunk bases (exclusive over c),
-//                       padding rows of row_to_slot set to -1
+//   2. permute_scan:    counts, padded offsets, chunk bases (exclusive over c)
 //   3. permute_scatter: row = offsets[e] + base[c][e] + rank
+// row_to_slot is set to -1 by a memset before the scatter fills the used rows.
 #include "internal.h"
 
 namespace moe {
@@ -62,8 +62,7 @@ __global__ void __launch_bounds__(kChunk) permute_count_kernel(const int* __rest
 // One block of 1024 threads; E <= 1024.
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int* __restrict__ hist, int C, int E,
                                                             int pad_m, int* __restrict__ counts,
-                                                            int* __restrict__ offsets,
-                                                            int* __restrict__ row_to_slot) {
+                                                            int* __restrict__ offsets) {
   __shared__ int warp_sums[32];
   const int e = threadIdx.x;
   int cnt = 0;
@@ -101,7 +100,6 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int* __restrict__ hi
   if (e < E) {
     offsets[e] = excl;
     if (e == E - 1) offsets[E] = excl + padded;
-    for (int r = excl + cnt; r < excl + padded; ++r) row_to_slot[r] = -1;
   }
 }
 
@@ -135,8 +133,8 @@ size_t permute_scratch_bytes(int T, int E) {
 }
 
 cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* counts,
-                           int* offsets, int* slot_to_row, int* row_to_slot, int* hist,
-                           int* status, cudaStream_t st) {
+                           int* offsets, int* slot_to_row, int* row_to_slot,
+                           int64_t rows_capacity, int* hist, int* status, cudaStream_t st) {
   const int C = (T + kChunk - 1) / kChunk;
   const size_t smem = size_t(kWarps) * E * sizeof(uint32_t);
   if (C > 0 && k > 0) {
@@ -144,10 +142,13 @@ cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* 
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
-  permute_scan_kernel<<<1, 1024, 0, st>>>(hist, (k > 0) ? C : 0, E, pad_m, counts, offsets,
-                                          row_to_slot);
+  permute_scan_kernel<<<1, 1024, 0, st>>>(hist, (k > 0) ? C : 0, E, pad_m, counts, offsets);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  if (rows_capacity > 0 && row_to_slot) {
+    err = cudaMemsetAsync(row_to_slot, 0xFF, size_t(rows_capacity) * sizeof(int), st);
+    if (err != cudaSuccess) return err;
+  }
   if (C > 0 && k > 0) {
     permute_scatter_kernel<<<C, kChunk, smem, st>>>(ids, T, E, k, hist, offsets, slot_to_row,
                                                     row_to_slot, status);

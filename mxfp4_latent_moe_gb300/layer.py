@@ -16,9 +16,9 @@ class MoeLayer:
     w2 u8 [E][d][I/2], w2_s u8 [E][d][I/32], all CUDA tensors.
     """
 
-    def __init__(self, w13, w13_s, w2, w2_s, k, pad_m=128, stream=None):
+    def __init__(self, w13, w13_s, w2, w2_s, k, kernel=abi.GEMM_AUTO, stream=None):
         E, two_i, half_d = w13.shape
-        self.E, self.I, self.d, self.k, self.pad_m = E, two_i // 2, half_d * 2, k, pad_m
+        self.E, self.I, self.d, self.k, self.kernel = E, two_i // 2, half_d * 2, k, kernel
         dev = w13.device
         self.w13, self.w2 = w13.contiguous(), w2.contiguous()
         self.w13_sf = torch.empty(abi.moe_tiled_scale_bytes(E * two_i, self.d), dtype=torch.uint8,
@@ -31,8 +31,12 @@ class MoeLayer:
     def weight_bytes_per_expert(self):
         return 3 * self.d * self.I // 2 + 3 * self.d * self.I // 32
 
+    def kernel_for(self, T):
+        """The grouped-GEMM kernel family a call with T tokens uses."""
+        return self.kernel or abi.moe_default_kernel(T, self.E, self.k)
+
     def workspace(self, T):
-        n = abi.moe_workspace_size(T, self.d, self.E, self.k, self.I, self.pad_m)
+        n = abi.moe_workspace_size(T, self.d, self.E, self.k, self.I)
         return torch.empty(n, dtype=torch.uint8, device=self.w13.device)
 
     def forward(self, x, logits, ws=None, y=None, topk_ids=None, topk_w=None, stream=None):
@@ -41,6 +45,6 @@ class MoeLayer:
             ws = self.workspace(T)
         if y is None:
             y = torch.empty(T, self.d, dtype=torch.bfloat16, device=x.device)
-        abi.moe_forward(T, self.d, self.E, self.k, self.I, self.pad_m, x, logits, self.w13,
+        abi.moe_forward(T, self.d, self.E, self.k, self.I, self.kernel_for(T), x, logits, self.w13,
                         self.w13_sf, self.w2, self.w2_sf, y, ws, topk_ids, topk_w, stream)
         return y

@@ -49,6 +49,9 @@ def test_size_helpers():
     assert abi.moe_rows_capacity(64, 896, 16, 128) == (1024 + 896 * 127 + 127) // 128 * 128
     assert abi.moe_rows_capacity(8, 32, 4, 128) == (32 + 32 * 127 + 127) // 128 * 128
     assert abi.moe_rows_capacity(8, 32, 4, 100) == -1    # not a power of two
+    assert abi.moe_default_kernel(64, 896, 16) == abi.GEMM_WEIGHT_TILES
+    assert abi.moe_default_kernel(512, 896, 16) == abi.GEMM_WEIGHT_TILES
+    assert abi.moe_default_kernel(8192, 896, 16) == abi.GEMM_TOKEN_TILES
     assert abi.moe_permute_workspace_size(0, 896) == 256
     assert abi.moe_permute_workspace_size(300, 896) == 256 + ((2 * 896 * 4 + 255) // 256) * 256
     ws = abi.moe_workspace_size(32768, 3584, 896, 16, 3072)
@@ -80,30 +83,34 @@ def test_host_validation_rejects_before_any_launch(L):
     assert _rc(L, "moe_quant_mxfp8", fake, 4, 100, None, 0, fake, fake, 128, None) == abi.UNSUPPORTED
     assert _rc(L, "moe_quant_mxfp8", ctypes.c_void_p(4098), 4, 256, None, 0, fake, fake, 128,
                None) == abi.INVALID_ARGUMENT
-    # GEMMs: pad other than 128, capacity not a multiple of 128, misaligned weights, no workspace
-    args = [fake, fake, fake, E, 3584, 3072]
-    assert _rc(L, "moe_grouped_gemm_w13_glu", *args, 16, fake, fake, fake, fake, 1024, fake, 256,
+    # GEMMs: unknown kernel, capacity not a multiple of 128, misaligned weights, no workspace
+    args = [fake, fake, fake, fake, E, 3584, 3072]
+    assert _rc(L, "moe_grouped_gemm_w13_glu", *args, 0, fake, fake, fake, fake, 1024, fake, 256,
                None) == abi.UNSUPPORTED
-    assert _rc(L, "moe_grouped_gemm_w13_glu", *args, 128, fake, fake, fake, fake, 1000, fake, 256,
+    assert _rc(L, "moe_grouped_gemm_w13_glu", *args, 1, fake, fake, fake, fake, 1000, fake, 256,
                None) == abi.UNSUPPORTED
-    assert _rc(L, "moe_grouped_gemm_w13_glu", *args, 128, ctypes.c_void_p(4096 + 16), fake, fake,
+    assert _rc(L, "moe_grouped_gemm_w13_glu", *args, 2, ctypes.c_void_p(4096 + 16), fake, fake,
                fake, 1024, fake, 256, None) == abi.INVALID_ARGUMENT
-    assert _rc(L, "moe_grouped_gemm_w13_glu", *args, 128, fake, fake, fake, fake, 1024, fake, 8,
+    assert _rc(L, "moe_grouped_gemm_w13_glu", *args, 1, fake, fake, fake, fake, 1024, fake, 8,
                None) == abi.WORKSPACE_TOO_SMALL
-    assert _rc(L, "moe_grouped_gemm_w2", fake, fake, fake, E, 3072, 3584, 128, fake, fake, None,
+    assert _rc(L, "moe_grouped_gemm_w13_glu", fake, fake, None, fake, E, 3584, 3072, 1, fake, fake,
+               fake, fake, 1024, fake, 256, None) == abi.INVALID_ARGUMENT   # counts required
+    assert _rc(L, "moe_grouped_gemm_w2", fake, fake, fake, fake, E, 3072, 3584, 1, fake, fake, None,
                1024, fake, 256, None) == abi.INVALID_ARGUMENT
     # combine: null output
     assert _rc(L, "moe_unpermute_combine", fake, fake, fake, 4, k, 3584, None, None) == \
         abi.INVALID_ARGUMENT
     # forward: dims null / unsupported
-    assert _rc(L, "moe_forward", None, 128, fake, fake, None, fake, None, None, fake, 10, None) == \
+    assert _rc(L, "moe_forward", None, 0, fake, fake, None, fake, None, None, fake, 10, None) == \
         abi.INVALID_ARGUMENT
     dims = abi._Dims(4, 3584, 896, 33, 3072)
-    assert _rc(L, "moe_forward", ctypes.byref(dims), 128, fake, fake, None, fake, None, None, fake,
+    assert _rc(L, "moe_forward", ctypes.byref(dims), 0, fake, fake, None, fake, None, None, fake,
                10, None) == abi.UNSUPPORTED
     dims = abi._Dims(4, 3584, 896, 16, 3072)
     W = abi._Weights(4096, 4096, 4096, 4096)
-    assert _rc(L, "moe_forward", ctypes.byref(dims), 128, fake, fake, ctypes.byref(W), fake, None,
+    assert _rc(L, "moe_forward", ctypes.byref(dims), 7, fake, fake, ctypes.byref(W), fake, None,
+               None, fake, 10 ** 9, None) == abi.UNSUPPORTED
+    assert _rc(L, "moe_forward", ctypes.byref(dims), 0, fake, fake, ctypes.byref(W), fake, None,
                None, fake, 10, None) == abi.WORKSPACE_TOO_SMALL
     # status helpers
     assert _rc(L, "moe_check_device_status", None, None) == abi.INVALID_ARGUMENT

@@ -23,8 +23,8 @@ def abi():
     return gu.cuda_lib()
 
 
-def _run_forward(abi, wl, L):
-    layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k)
+def _run_forward(abi, wl, L, kernel=0):
+    layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k, kernel=kernel)
     ws = layer.workspace(wl.T)
     ids = torch.empty(wl.T, max(wl.k, 1), dtype=torch.int32, device="cuda")
     w = torch.empty(wl.T, max(wl.k, 1), dtype=torch.float32, device="cuda")
@@ -45,9 +45,10 @@ def _host_layer(L):
     synth.shape("one_expert", T=130, d=256, E=1, k=1, I=256),
     synth.shape("all_experts", T=20, d=128, E=8, k=8, I=128),
 ])
-def test_forward_small_all_outputs(abi, orc, wl):
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_forward_small_all_outputs(abi, orc, wl, kernel):
     L = synth.make_layer(wl, seed=0, device="cuda")
-    y, ids, w = _run_forward(abi, wl, L)
+    y, ids, w = _run_forward(abi, wl, L, kernel)
     H = _host_layer(L)
     ref = orc.moe_forward(synth.bf16_bits(L["x"]), L["logits"].cpu().numpy(), wl.k, H["w13"],
                           H["w13_s"], H["w2"], H["w2_s"], want_y64=True)
@@ -85,6 +86,7 @@ def _sample_tokens(wl, L, n):
 @pytest.mark.parametrize("name", ["decode_t64", "decode_t512", "prefill_skewed_t8192",
                                   "prefill_outlier_t32768"])
 def test_forward_full_size_workloads(abi, orc, name):
+    """The benchmark's configuration: kernel family chosen by moe_default_kernel."""
     wl = synth.workload(name)
     L = synth.make_layer(wl, seed=0, device="cuda")
     y, ids, w = _run_forward(abi, wl, L)
@@ -94,15 +96,16 @@ def test_forward_full_size_workloads(abi, orc, name):
     assert np.array_equal(ids.cpu().numpy(), rids)
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
     # grouping: every slot, through the step entry point
-    rc = abi.moe_rows_capacity(wl.T, wl.E, wl.k, 128)
+    pad = 128
+    rc = abi.moe_rows_capacity(wl.T, wl.E, wl.k, pad)
     counts = torch.empty(wl.E, dtype=torch.int32, device="cuda")
     offsets = torch.empty(wl.E + 1, dtype=torch.int32, device="cuda")
     s2r = torch.empty(wl.T * wl.k, dtype=torch.int32, device="cuda")
     r2s = torch.empty(rc, dtype=torch.int32, device="cuda")
     pws = torch.zeros(abi.moe_permute_workspace_size(wl.T, wl.E), dtype=torch.uint8, device="cuda")
-    abi.moe_permute(ids.contiguous(), wl.T, wl.E, wl.k, 128, counts, offsets, s2r, r2s, rc, pws)
+    abi.moe_permute(ids.contiguous(), wl.T, wl.E, wl.k, pad, counts, offsets, s2r, r2s, rc, pws)
     assert abi.moe_check_device_status(pws) == 0
-    rperm = orc.permute(rids, wl.E, 128)
+    rperm = orc.permute(rids, wl.E, pad)
     assert np.array_equal(offsets.cpu().numpy(), rperm["offsets"])
     assert np.array_equal(s2r.cpu().numpy(), rperm["slot_to_row"])
     # sampled tokens: MXFP8 codes of x at every grouped row, and the layer output

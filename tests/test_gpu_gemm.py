@@ -1,7 +1,9 @@
 """GPU parity of the two grouped GEMMs (tcgen05 block-scaled MMA) against the
 oracle's per-expert stage functions, on ragged expert groups: empty groups,
 groups of 1, 15..17, 127..129 and several hundred rows, K not a multiple of the
-pipeline depth, and more tiles than SMs."""
+pipeline depth, and more tiles than SMs. Both kernel families: token tiles
+(tokens on the MMA's M side) and weight tiles (weights on the M side, an
+expert's tokens as N = its count rounded up to 32, at most 128 per tile)."""
 import numpy as np
 import pytest
 import torch
@@ -22,7 +24,8 @@ def _groups(sizes):
     for c in sizes:
         offsets.append(offsets[-1] + (c + 127) // 128 * 128)
     rows = [(e, offsets[e] + i) for e, c in enumerate(sizes) for i in range(c)]
-    return np.array(offsets, np.int32), rows, max(offsets[-1], 128)
+    return (np.array(sizes, np.int32), np.array(offsets, np.int32), rows,
+            max(offsets[-1], 128))
 
 
 def _dev(a):
@@ -54,14 +57,15 @@ def _check_mxfp8_rows(got_c, got_s, ref_c, ref_s):
 
 CASES = [
     ([0, 1, 15, 16, 17, 127, 128, 129, 300], 256, 256),
-    ([3, 0, 250, 130], 384, 384),
+    ([3, 0, 250, 130, 33, 64, 96, 65], 384, 384),
     (list(np.random.default_rng(0).integers(0, 300, 40)), 256, 512),
 ]
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("sizes,d,I", CASES)
-def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I):
-    offsets, rows, rc = _groups(sizes)
+def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel):
+    counts, offsets, rows, rc = _groups(sizes)
     E = len(sizes)
     W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=1)
     xq = synth.random_e4m3_codes((rc, d), seed=2).numpy()
@@ -69,7 +73,8 @@ def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I):
     hq = torch.zeros(rc, I, dtype=torch.uint8, device="cuda")
     hs = torch.zeros(abi.moe_tiled_scale_bytes(rc, I), dtype=torch.uint8, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    abi.moe_grouped_gemm_w13_glu(_dev(xq), _dev(gu.tile(xs, d)), _dev(offsets), E, d, I, 128,
+    abi.moe_grouped_gemm_w13_glu(_dev(xq), _dev(gu.tile(xs, d)), _dev(counts), _dev(offsets), E, d,
+                                 I, kernel,
                                  W["w13"].cuda(), _prepacked(abi, W["w13_s"].numpy(), E * 2 * I, d),
                                  hq, hs, rc, ws)
     assert abi.moe_check_device_status(ws) == 0
@@ -82,16 +87,18 @@ def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I):
     _check_mxfp8_rows(got_c[idx], got_s[idx], ref_c, ref_s)
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("sizes,d,I", CASES)
-def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I):
-    offsets, rows, rc = _groups(sizes)
+def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I, kernel):
+    counts, offsets, rows, rc = _groups(sizes)
     E = len(sizes)
     W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=4)
     hq = synth.random_e4m3_codes((rc, I), seed=5).numpy()
     hs = synth.random_scale_codes((rc, I // 32), lo=118, hi=130, seed=6).numpy()
     yp = torch.zeros(rc, d, dtype=torch.bfloat16, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    abi.moe_grouped_gemm_w2(_dev(hq), _dev(gu.tile(hs, I)), _dev(offsets), E, I, d, 128,
+    abi.moe_grouped_gemm_w2(_dev(hq), _dev(gu.tile(hs, I)), _dev(counts), _dev(offsets), E, I, d,
+                            kernel,
                             W["w2"].cuda(), _prepacked(abi, W["w2_s"].numpy(), E * d, I), yp, rc,
                             ws)
     assert abi.moe_check_device_status(ws) == 0
@@ -102,3 +109,24 @@ def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I):
     rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
     err = np.abs(got[idx] - ref)
     assert np.all(err <= np.abs(ref) * 2.0 ** -8 + 1e-5 * rms), float((err / (rms + 1e-30)).max())
+
+
+def test_gemm_refuses_bad_groups(abi):
+    d = I = 256
+    W = synth.make_weights(synth.shape("g", T=1, d=d, E=2, k=1, I=I), seed=1)
+    rc = 256
+    xq = torch.zeros(rc, d, dtype=torch.uint8, device="cuda")
+    xs = torch.zeros(abi.moe_tiled_scale_bytes(rc, d), dtype=torch.uint8, device="cuda")
+    hq = torch.full((rc, I), 0x5A, dtype=torch.uint8, device="cuda")
+    hs = torch.zeros(abi.moe_tiled_scale_bytes(rc, I), dtype=torch.uint8, device="cuda")
+    w13_sf = _prepacked(abi, W["w13_s"].numpy(), 2 * 2 * I, d)
+    bad = [(np.array([48, 48], np.int32), np.array([0, 48, 96], np.int32)),     # not padded to 128
+           (np.array([130, 0], np.int32), np.array([0, 128, 256], np.int32)),   # count > group
+           (np.array([1, 1], np.int32), np.array([0, 128, 384], np.int32))]     # past the capacity
+    for counts, offsets in bad:
+        for kernel in (1, 2):
+            ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+            abi.moe_grouped_gemm_w13_glu(xq, xs, _dev(counts), _dev(offsets), 2, d, I, kernel,
+                                         W["w13"].cuda(), w13_sf, hq, hs, rc, ws)
+            assert abi.moe_check_device_status(ws) == 6       # MOE_ERR_DEVICE_BAD_INPUT
+    assert bool((hq == 0x5A).all())                           # nothing written
