@@ -124,9 +124,10 @@ int32_t moe_abi_version(void);
  * to a multiple of 128). Returns 0 for unsupported K. */
 size_t moe_tiled_scale_bytes(int64_t rows, int32_t K);
 
-/* The GEMM kernels moe_forward uses for MOE_GEMM_AUTO: MOE_GEMM_WEIGHT_TILES
- * while T*k < 64*E (fewer than 64 tokens per expert on average), else
- * MOE_GEMM_TOKEN_TILES. Returns -1 for an unsupported shape. */
+/* The GEMM kernels moe_forward uses for MOE_GEMM_AUTO: currently
+ * MOE_GEMM_TOKEN_TILES for every shape (on GB300 it streams the weights
+ * faster than MOE_GEMM_WEIGHT_TILES even at 64 tokens). Returns -1 for an
+ * unsupported shape. */
 int32_t moe_default_kernel(int32_t T, int32_t E, int32_t k);
 
 /* Rows a grouped activation buffer needs for T tokens, k experts each, E
