@@ -169,6 +169,32 @@ moe_status moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k,
                        int32_t* row_to_slot, int64_t rows_capacity, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
 
+/* Allocation-free variant of moe_permute. The pages have no counterpart: it
+ * exists for callers that cannot hand the library device memory for a
+ * workspace -- a host framework that owns every device allocation through its
+ * own pool and forbids libraries to allocate, or a latency-critical caller that
+ * must not call cudaMalloc on its serving path (it may synchronise the whole
+ * device). Same arguments, results and rules as moe_permute, without ws:
+ *  - The per-chunk histograms live in a fixed 1 MiB device array inside
+ *    libmoe.so, held by every GPU that loads the library until the process
+ *    exits. Calls need ceil(T/256) * E * 4 <= 1 MiB (T <= 74,752 at E = 896);
+ *    larger calls return MOE_ERR_WORKSPACE_TOO_SMALL and enqueue nothing.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress) and caches it; make that
+ *    first call before any stream capture. Nothing here calls cudaMalloc,
+ *    cudaFree or any other allocating routine.
+ *  - All calls share the array and it keeps the previous call's contents;
+ *    every byte a call reads it has written first, so no clearing is needed.
+ *    Calls that overlap on the GPU (other streams, other host threads) race
+ *    on it: serialise them.
+ *  - status: optional device int32 (NULL = none) that receives
+ *    MOE_ERR_DEVICE_BAD_INPUT for an id out of range or repeated within a
+ *    token (first error wins; the caller clears it). */
+moe_status moe_permute_noalloc(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k,
+                               int32_t pad_m, int32_t* counts, int32_t* offsets,
+                               int32_t* slot_to_row, int32_t* row_to_slot, int64_t rows_capacity,
+                               int32_t* status, cudaStream_t stream);
+
 /* MXFP8 quantisation of the stage-1 activations (OCP MX rule, E4M3 + E8M0
  * per 32 consecutive values of a row): per block, scale code
  * c = clamp(floor(log2(amax)) - 8 + 127, 0, 254) (0 for an all-zero block),

@@ -48,6 +48,7 @@ _SIGS = {
     "moe_route_topk": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_permute_workspace_size": (_sz, [_i32, _i32]),
     "moe_permute": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
+    "moe_permute_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
     "moe_quant_mxfp8": (_i32, [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _i64, _vp]),
     "moe_grouped_gemm_w13_glu": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                         _vp, _i64, _vp, _sz, _vp]),
@@ -155,6 +156,13 @@ def moe_permute(topk_ids, T, E, k, pad_m, counts, offsets, slot_to_row, row_to_s
     _call("moe_permute", _ptr(topk_ids), T, E, k, pad_m, _ptr(counts), _ptr(offsets),
           _ptr(slot_to_row), _ptr(row_to_slot), rows_capacity, _ptr(ws), ws.numel() * ws.element_size(),
           _stream(stream))
+
+
+def moe_permute_noalloc(topk_ids, T, E, k, pad_m, counts, offsets, slot_to_row, row_to_slot,
+                        rows_capacity, status=None, stream=None):
+    """moe_permute without a workspace (for callers that cannot allocate one)."""
+    _call("moe_permute_noalloc", _ptr(topk_ids), T, E, k, pad_m, _ptr(counts), _ptr(offsets),
+          _ptr(slot_to_row), _ptr(row_to_slot), rows_capacity, _ptr(status), _stream(stream))
 
 
 def moe_quant_mxfp8(x, T, d, slot_to_row, k, codes, scales, rows_capacity, stream=None):

@@ -13,6 +13,8 @@
 //   2. permute_scan:    counts, padded offsets, chunk bases (exclusive over c)
 //   3. permute_scatter: row = offsets[e] + base[c][e] + rank
 // row_to_slot is set to -1 by a memset before the scatter fills the used rows.
+#include <mutex>
+
 #include "internal.h"
 
 namespace moe {
@@ -158,3 +160,75 @@ cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* 
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free grouping (moe_permute_noalloc).
+//
+// moe_permute keeps its per-chunk expert histograms in a workspace the caller
+// allocates. Some callers cannot do that: a host framework that owns every
+// byte of device memory through its own pool and forbids libraries to
+// allocate, or a latency-critical caller that must not call cudaMalloc on its
+// serving path because cudaMalloc may synchronise the whole device. For them
+// the histograms live in the fixed device array below, part of this library's
+// image: every GPU that loads the library holds its 1 MiB until the process
+// exits. Its device address is looked up once per device (the first call on
+// that device, with that device current) and cached.
+// ---------------------------------------------------------------------------
+namespace moe {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // histograms of ceil(T/256) x E ints
+static __device__ __align__(256) unsigned char g_permute_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_permute_scratch on the current device, or nullptr.
+void* scratch_on_current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return nullptr;
+    g_scratch_ptr[dev] = p;
+  }
+  return g_scratch_ptr[dev];
+}
+
+bool is_aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+
+}  // namespace moe
+
+extern "C" moe_status moe_permute_noalloc(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k,
+                                          int32_t pad_m, int32_t* counts, int32_t* offsets,
+                                          int32_t* slot_to_row, int32_t* row_to_slot,
+                                          int64_t rows_capacity, int32_t* status,
+                                          cudaStream_t stream) {
+  if (T < 0 || E < 0 || k < 0 || rows_capacity < 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (E < 1 || E > 1024 || k > 32 || k > E || int64_t(T) * k >= int64_t(INT32_MAX))
+    return MOE_ERR_UNSUPPORTED;
+  if (pad_m < 1 || pad_m > 1024 || (pad_m & (pad_m - 1)) != 0) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !moe::is_aligned4(counts) || !moe::is_aligned4(offsets))
+    return MOE_ERR_INVALID_ARGUMENT;
+  const bool any = T > 0 && k > 0;
+  if (any && (!topk_ids || !slot_to_row || !row_to_slot || !moe::is_aligned4(topk_ids) ||
+              !moe::is_aligned4(slot_to_row) || !moe::is_aligned4(row_to_slot)))
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (status && !moe::is_aligned4(status)) return MOE_ERR_INVALID_ARGUMENT;
+  const int64_t slots = int64_t(T) * k;
+  if (rows_capacity < slots + (slots < E ? slots : int64_t(E)) * (pad_m - 1))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (moe::permute_scratch_bytes(T, E) > moe::kNoAllocScratchBytes)
+    return MOE_ERR_WORKSPACE_TOO_SMALL;  // more token chunks x experts than the fixed array holds
+  void* scratch = moe::scratch_on_current_device();
+  if (!scratch) return MOE_ERR_CUDA;
+  const cudaError_t e =
+      moe::launch_permute(topk_ids, T, E, k, pad_m, counts, offsets, slot_to_row, row_to_slot,
+                          rows_capacity, static_cast<int*>(scratch), status, stream);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
