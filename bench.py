@@ -245,9 +245,11 @@ def main():
     counts = torch.bincount(ids.reshape(-1).long(), minlength=E)
     U = int((counts > 0).sum())
     valid_rows = T * k
-    rows_cap = abi.moe_rows_capacity(T, E, k, 128)
     kernel = layer.kernel_for(T)
-    padded_rows = int(((counts + 127) // 128 * 128).sum())
+    pad = 32 if kernel == abi.GEMM_WEIGHT_TILES else 128
+    layout = abi.SCALES_GROUP32 if kernel == abi.GEMM_WEIGHT_TILES else abi.SCALES_TILED128
+    rows_cap = abi.moe_rows_capacity(T, E, k, pad)
+    padded_rows = int(((counts + pad - 1) // pad * pad).sum())
     expert_bytes = layer.weight_bytes_per_expert()
     w13_bytes = 2 * I * d // 2 + 2 * I * d // 32
     w2_bytes = d * I // 2 + d * I // 32
@@ -302,16 +304,16 @@ def main():
     r2s = torch.empty(rc, dtype=torch.int32, device=dev)
     pws = torch.zeros(abi.moe_permute_workspace_size(T, E), dtype=torch.uint8, device=dev)
     xq = torch.empty(rc, d, dtype=torch.uint8, device=dev)
-    xs = torch.empty(abi.moe_tiled_scale_bytes(rc, d), dtype=torch.uint8, device=dev)
+    xs = torch.empty(abi.moe_activation_scale_bytes(rc, d, layout), dtype=torch.uint8, device=dev)
     hq = torch.empty(rc, I, dtype=torch.uint8, device=dev)
-    hs = torch.empty(abi.moe_tiled_scale_bytes(rc, I), dtype=torch.uint8, device=dev)
+    hs = torch.empty(abi.moe_activation_scale_bytes(rc, I, layout), dtype=torch.uint8, device=dev)
     yp = torch.empty(rc, d, dtype=torch.bfloat16, device=dev)
     gws = torch.zeros(256, dtype=torch.uint8, device=dev)
     names = ["route_topk", "permute", "quant_mxfp8", "gemm_w13_glu", "gemm_w2", "combine"]
     calls = [
         lambda: abi.moe_route_topk(logits, T, E, k, ids, w),
-        lambda: abi.moe_permute(ids, T, E, k, 128, counts_d, offsets_d, s2r, r2s, rc, pws),
-        lambda: abi.moe_quant_mxfp8(x, T, d, s2r, k, xq, xs, rc),
+        lambda: abi.moe_permute(ids, T, E, k, pad, counts_d, offsets_d, s2r, r2s, rc, pws),
+        lambda: abi.moe_quant_mxfp8(x, T, d, s2r, k, xq, xs, rc, layout),
         lambda: abi.moe_grouped_gemm_w13_glu(xq, xs, counts_d, offsets_d, E, d, I, kernel,
                                              layer.w13, layer.w13_sf, hq, hs, rc, gws),
         lambda: abi.moe_grouped_gemm_w2(hq, hs, counts_d, offsets_d, E, I, d, kernel, layer.w2,

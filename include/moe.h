@@ -36,18 +36,18 @@
  * Shapes (checked; anything else is MOE_ERR_UNSUPPORTED):
  *   1 <= E <= 1024, 0 <= k <= min(E, 32), T >= 0, T*k < 2^31,
  *   d % 128 == 0 and I % 128 == 0 (both >= 128),
- *   grouped GEMMs and moe_forward: expert groups padded to 128 rows
- *   (moe_permute with pad_m = 128); moe_permute itself takes any power of two
- *   1..1024.
+ *   moe_permute takes any power of two 1..1024 as pad_m.
  *
  * Two kernel families run the grouped GEMMs (moe_gemm_kernel):
  *   MOE_GEMM_TOKEN_TILES   tokens are the MMA's M side (128-row tiles),
  *                          weights the N side; for many tokens per expert.
+ *                          Groups padded to 128 rows; activation scales in
+ *                          the TILED layout.
  *   MOE_GEMM_WEIGHT_TILES  weights are the M side (128 weight rows per MMA),
- *                          an expert's tokens the N side (its count rounded up
- *                          to 32, at most 128 per tile); for a few tokens per
- *                          expert (decode), where streaming the weights from
- *                          HBM is the bound.
+ *                          an expert's tokens the N side in chunks of 32; for
+ *                          a few tokens per expert (decode), where streaming
+ *                          the weights from HBM is the bound. Groups padded to
+ *                          32 rows; activation scales in the GROUP32 layout.
  *
  * Data layouts:
  *   x, y        bf16 [T][d] row-major.
@@ -65,6 +65,10 @@
  *     ((r/128)*(K/128) + b/4)*512 + (r%32)*16 + ((r/32)%4)*4 + b%4,
  *   i.e. one 512-byte atom per 128 rows x 128 inputs, in the order the
  *   tensor-core scale-factor copy reads it.
+ *   GROUP32 scale layout (activations of the weight-tile GEMMs): one 512-byte
+ *   block per 32 rows x 128 inputs; the scale of row r, 32-block b is byte
+ *     ((r/32)*(K/128) + b/4)*512 + (r%32)*16 + b%4,
+ *   the other 12 bytes of each 16 unused (rows * K / 8 bytes in all).
  *   Grouped rows: rows [offsets[e], offsets[e+1]) belong to expert e, the
  *   first counts[e] of them hold its tokens in ascending token order, the rest
  *   are padding (row_to_slot == -1, contents unspecified, never read back).
@@ -89,6 +93,11 @@ typedef enum {
   MOE_ERR_DEVICE_TIMEOUT = 5,      /* device status: a bounded wait ran out */
   MOE_ERR_DEVICE_BAD_INPUT = 6     /* device status: expert id out of range or repeated */
 } moe_status;
+
+typedef enum {
+  MOE_SCALES_TILED128 = 0,   /* activation scales for the token-tile GEMMs */
+  MOE_SCALES_GROUP32 = 1     /* activation scales for the weight-tile GEMMs */
+} moe_scale_layout;
 
 typedef enum {
   MOE_GEMM_AUTO = 0,         /* moe_forward only: see moe_default_kernel */
@@ -129,6 +138,11 @@ size_t moe_tiled_scale_bytes(int64_t rows, int32_t K);
  * faster than MOE_GEMM_WEIGHT_TILES even at 64 tokens). Returns -1 for an
  * unsupported shape. */
 int32_t moe_default_kernel(int32_t T, int32_t E, int32_t k);
+
+/* Bytes of an activation scale array for `rows` rows of K inputs in the given
+ * moe_scale_layout (rows rounded up to 128 or 32). 0 for unsupported K or
+ * layout. */
+size_t moe_activation_scale_bytes(int64_t rows, int32_t K, int32_t scale_layout);
 
 /* Rows a grouped activation buffer needs for T tokens, k experts each, E
  * experts and padding pad_m: T*k + min(E, T*k)*(pad_m-1), rounded up to 128. */
@@ -202,11 +216,12 @@ moe_status moe_permute_noalloc(const int32_t* topk_ids, int32_t T, int32_t E, in
  * +-448, the sign kept on zero results.
  * x bf16 [T][d]. With slot_to_row == NULL the output rows are the tokens
  * (row t); otherwise token t is written to every row slot_to_row[t*k + j],
- * j < k. codes u8 [rows_capacity][d]; scales TILED for (rows_capacity, d).
- * rows_capacity % 128 == 0. */
+ * j < k. codes u8 [rows_capacity][d]; scales in scale_layout (moe_scale_layout:
+ * TILED for the token-tile GEMMs, GROUP32 for the weight-tile GEMMs) for
+ * (rows_capacity, d). rows_capacity % 128 == 0. */
 moe_status moe_quant_mxfp8(const uint16_t* x, int32_t T, int32_t d, const int32_t* slot_to_row,
-                           int32_t k, uint8_t* codes, uint8_t* scales, int64_t rows_capacity,
-                           cudaStream_t stream);
+                           int32_t k, uint8_t* codes, uint8_t* scales, int32_t scale_layout,
+                           int64_t rows_capacity, cudaStream_t stream);
 
 /* Stage 1 grouped GEMM on tcgen05 block-scaled tensor cores
  * (kind::mxf8f6f4, MXFP8 activations x MXFP4 weights, fp32 accumulation)
@@ -215,16 +230,17 @@ moe_status moe_quant_mxfp8(const uint16_t* x, int32_t T, int32_t d, const int32_
  * For each expert e and each of its grouped rows r:
  *   g = X[r] . W1[e]^T, u = X[r] . W3[e]^T  (dequantised operands, fp32 sums)
  *   h = silu(g) * u (fp32), then MXFP8 as in moe_quant_mxfp8
- *   -> hq [r][I] codes and hs TILED scales for (rows_capacity, I).
+ *   -> hq [r][I] codes and hs scales for (rows_capacity, I).
+ * kernel: MOE_GEMM_TOKEN_TILES (xs and hs TILED, groups padded to 128) or
+ * MOE_GEMM_WEIGHT_TILES (xs and hs GROUP32, groups padded to 32).
  * counts int32 [E] and offsets int32 [E+1] are read on the device and must
- * come from moe_permute with pad_m = 128: every group a multiple of 128 rows
+ * come from moe_permute with that padding: every group a multiple of it
  * holding counts[e] tokens, offsets[0] == 0, offsets[E] <= rows_capacity.
  * Offsets or counts that break this are refused on the device
  * (MOE_ERR_DEVICE_BAD_INPUT in the status word, nothing written).
- * MOE_GEMM_TOKEN_TILES computes every row of each group (padding rows hold
- * unspecified values); MOE_GEMM_WEIGHT_TILES computes the first counts[e]
- * rows rounded up to 32 and leaves the rest untouched.
- * kernel: MOE_GEMM_TOKEN_TILES or MOE_GEMM_WEIGHT_TILES.
+ * Each family computes the group rows that hold tokens, in whole tiles (128
+ * or 32 rows): padding rows inside a tile hold unspecified values, later
+ * padding rows are left untouched.
  * ws: at least MOE_STATUS_BYTES; the status word records timeouts.
  * xq, hq 16-byte aligned; w13 32-byte aligned; scale arrays 16-byte aligned. */
 moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int32_t* counts,
@@ -236,7 +252,8 @@ moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const 
 /* Stage 2 grouped GEMM (the down projection w2, 3,072 -> 3,584 in the pages'
  * layer): Yp[r] = H[r] . W2[e]^T with MXFP8 H and MXFP4 W2 on tcgen05
  * block-scaled tensor cores, fp32 accumulation, rounded to bf16.
- * yp bf16 [rows_capacity][d], 16-byte aligned. Other arguments as above. */
+ * yp bf16 [rows_capacity][d], 16-byte aligned; hq, hs, counts, offsets and
+ * kernel as produced for / by the stage-1 call. */
 moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32_t* counts,
                                const int32_t* offsets, int32_t E, int32_t I, int32_t d,
                                int32_t kernel, const uint8_t* w2, const uint8_t* w2_sf,

@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 STATUS_BYTES = 256
 OK, INVALID_ARGUMENT, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA, DEVICE_TIMEOUT, DEVICE_BAD_INPUT = range(7)
 GEMM_AUTO, GEMM_TOKEN_TILES, GEMM_WEIGHT_TILES = range(3)
+SCALES_TILED128, SCALES_GROUP32 = range(2)
 
 
 class MoeError(RuntimeError):
@@ -42,6 +43,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_i32]),
     "moe_abi_version": (_i32, []),
     "moe_tiled_scale_bytes": (_sz, [_i64, _i32]),
+    "moe_activation_scale_bytes": (_sz, [_i64, _i32, _i32]),
     "moe_rows_capacity": (_i64, [_i32, _i32, _i32, _i32]),
     "moe_default_kernel": (_i32, [_i32, _i32, _i32]),
     "moe_prepack_scales": (_i32, [_vp, _i64, _i32, _vp, _vp]),
@@ -49,7 +51,7 @@ _SIGS = {
     "moe_permute_workspace_size": (_sz, [_i32, _i32]),
     "moe_permute": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
     "moe_permute_noalloc": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
-    "moe_quant_mxfp8": (_i32, [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _i64, _vp]),
+    "moe_quant_mxfp8": (_i32, [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _i32, _i64, _vp]),
     "moe_grouped_gemm_w13_glu": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                         _vp, _i64, _vp, _sz, _vp]),
     "moe_grouped_gemm_w2": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _i64,
@@ -122,6 +124,10 @@ def moe_tiled_scale_bytes(rows, K):
     return lib().moe_tiled_scale_bytes(rows, K)
 
 
+def moe_activation_scale_bytes(rows, K, layout):
+    return lib().moe_activation_scale_bytes(rows, K, layout)
+
+
 def moe_rows_capacity(T, E, k, pad_m):
     return lib().moe_rows_capacity(T, E, k, pad_m)
 
@@ -165,9 +171,10 @@ def moe_permute_noalloc(topk_ids, T, E, k, pad_m, counts, offsets, slot_to_row, 
           _ptr(slot_to_row), _ptr(row_to_slot), rows_capacity, _ptr(status), _stream(stream))
 
 
-def moe_quant_mxfp8(x, T, d, slot_to_row, k, codes, scales, rows_capacity, stream=None):
+def moe_quant_mxfp8(x, T, d, slot_to_row, k, codes, scales, rows_capacity, scale_layout=0,
+                    stream=None):
     _call("moe_quant_mxfp8", _ptr(x), T, d, _ptr(slot_to_row), k, _ptr(codes), _ptr(scales),
-          rows_capacity, _stream(stream))
+          scale_layout, rows_capacity, _stream(stream))
 
 
 def moe_grouped_gemm_w13_glu(xq, xs, counts, offsets, E, d, I, kernel, w13, w13_sf, hq, hs,

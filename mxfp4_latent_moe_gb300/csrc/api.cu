@@ -10,7 +10,12 @@ using moe::tiled_sf_offset;
 
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
-constexpr int kGroupPad = 128;  // grouped rows: every expert's group is a multiple of 128
+// Expert groups: multiples of 128 rows for token tiles, of 32 for weight tiles
+// (whose activation scales use the GROUP32 layout).
+int32_t group_pad(int32_t kernel) { return kernel == MOE_GEMM_WEIGHT_TILES ? 32 : 128; }
+int32_t scale_layout(int32_t kernel) {
+  return kernel == MOE_GEMM_WEIGHT_TILES ? MOE_SCALES_GROUP32 : MOE_SCALES_TILED128;
+}
 
 bool kernel_ok(int32_t kernel) {
   return kernel == MOE_GEMM_TOKEN_TILES || kernel == MOE_GEMM_WEIGHT_TILES;
@@ -61,13 +66,23 @@ size_t tiled_bytes(int64_t rows, int32_t K) {
   return size_t(rp) * size_t(K / 32);
 }
 
+size_t group32_bytes(int64_t rows, int32_t K) {
+  const int64_t rp = (rows + 31) / 32 * 32;
+  return size_t(rp) * size_t(K / 8);
+}
+
+size_t act_scale_bytes(int64_t rows, int32_t K, int32_t layout) {
+  return layout == MOE_SCALES_GROUP32 ? group32_bytes(rows, K) : tiled_bytes(rows, K);
+}
+
 struct ForwardLayout {
   size_t status, hist, ids, w, counts, offsets, s2r, r2s, xq, xs, hq, hs, yp, total;
   int64_t rows_cap;
 };
 
-ForwardLayout forward_layout(const moe_dims& D) {
-  const int32_t pad_m = kGroupPad;
+ForwardLayout forward_layout(const moe_dims& D, int32_t kernel) {
+  const int32_t pad_m = group_pad(kernel);
+  const int32_t layout = scale_layout(kernel);
   ForwardLayout L{};
   const size_t slots = size_t(D.T) * size_t(D.k);
   L.rows_cap = rows_capacity_of(D.T, D.E, D.k, pad_m);
@@ -87,9 +102,9 @@ ForwardLayout forward_layout(const moe_dims& D) {
   L.s2r = take(slots * 4);
   L.r2s = take(rc * 4);
   L.xq = take(rc * size_t(D.d));
-  L.xs = take(tiled_bytes(L.rows_cap, D.d));
+  L.xs = take(act_scale_bytes(L.rows_cap, D.d, layout));
   L.hq = take(rc * size_t(D.I));
-  L.hs = take(tiled_bytes(L.rows_cap, D.I));
+  L.hs = take(act_scale_bytes(L.rows_cap, D.I, layout));
   L.yp = take(rc * size_t(D.d) * 2);
   L.total = off;
   return L;
@@ -155,6 +170,12 @@ size_t moe_tiled_scale_bytes(int64_t rows, int32_t K) {
   return tiled_bytes(rows, K);
 }
 
+size_t moe_activation_scale_bytes(int64_t rows, int32_t K, int32_t scale_layout) {
+  if (rows < 0 || check_width(K) != MOE_OK) return 0;
+  if (scale_layout != MOE_SCALES_TILED128 && scale_layout != MOE_SCALES_GROUP32) return 0;
+  return act_scale_bytes(rows, K, scale_layout);
+}
+
 int32_t moe_default_kernel(int32_t T, int32_t E, int32_t k) {
   if (check_routing_shape(T, E, k) != MOE_OK) return -1;
   return auto_kernel(T, E, k);
@@ -214,20 +235,23 @@ moe_status moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k,
 }
 
 moe_status moe_quant_mxfp8(const uint16_t* x, int32_t T, int32_t d, const int32_t* slot_to_row,
-                           int32_t k, uint8_t* codes, uint8_t* scales, int64_t rows_capacity,
-                           cudaStream_t stream) {
+                           int32_t k, uint8_t* codes, uint8_t* scales, int32_t scale_layout,
+                           int64_t rows_capacity, cudaStream_t stream) {
   if (T < 0 || k < 0 || rows_capacity < 0) return MOE_ERR_INVALID_ARGUMENT;
   moe_status s = check_width(d);
   if (s != MOE_OK) return s;
   if (k > kMaxK || int64_t(T) * (k > 0 ? k : 1) >= int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
   if (rows_capacity % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (scale_layout != MOE_SCALES_TILED128 && scale_layout != MOE_SCALES_GROUP32)
+    return MOE_ERR_UNSUPPORTED;
   if (T == 0 || (slot_to_row && k == 0)) return MOE_OK;
   if (!x || !codes || !scales) return MOE_ERR_INVALID_ARGUMENT;
   if (!aligned(x, 16) || !aligned(codes, 8) || !aligned(scales, 4) ||
       (slot_to_row && !aligned(slot_to_row, 4)))
     return MOE_ERR_INVALID_ARGUMENT;
   if (!slot_to_row && rows_capacity < T) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  return from_cuda(moe::launch_quant_mxfp8(x, T, d, slot_to_row, k, codes, scales, stream));
+  return from_cuda(
+      moe::launch_quant_mxfp8(x, T, d, slot_to_row, k, codes, scales, scale_layout, stream));
 }
 
 moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int32_t* counts,
@@ -282,7 +306,9 @@ moe_status moe_workspace_size(const moe_dims* dims, size_t* bytes) {
   if (!bytes) return MOE_ERR_INVALID_ARGUMENT;
   moe_status s = check_dims(dims);
   if (s != MOE_OK) return s;
-  *bytes = forward_layout(*dims).total;
+  const size_t a = forward_layout(*dims, MOE_GEMM_TOKEN_TILES).total;
+  const size_t b = forward_layout(*dims, MOE_GEMM_WEIGHT_TILES).total;
+  *bytes = a > b ? a : b;
   return MOE_OK;
 }
 
@@ -294,7 +320,7 @@ moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
   if (s != MOE_OK) return s;
   if (kernel == MOE_GEMM_AUTO) kernel = auto_kernel(dims->T, dims->E, dims->k);
   if (!kernel_ok(kernel)) return MOE_ERR_UNSUPPORTED;
-  const int32_t pad_m = kGroupPad;
+  const int32_t pad_m = group_pad(kernel);
   const moe_dims D = *dims;
   if (D.T == 0) return MOE_OK;
   if (!x || !logits || !W || !y || !ws || !W->w13 || !W->w13_sf || !W->w2 || !W->w2_sf)
@@ -304,7 +330,7 @@ moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
       !aligned(W->w2_sf, 16) || (topk_ids_out && !aligned(topk_ids_out, 4)) ||
       (topk_w_out && !aligned(topk_w_out, 4)))
     return MOE_ERR_INVALID_ARGUMENT;
-  const ForwardLayout L = forward_layout(D);
+  const ForwardLayout L = forward_layout(D, kernel);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
 
   int* status = at<int>(ws, L.status);
@@ -329,7 +355,8 @@ moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
   if ((e = moe::launch_permute(ids, D.T, D.E, D.k, pad_m, counts, offsets, s2r, r2s, L.rows_cap,
                                at<int>(ws, L.hist), status, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if ((e = moe::launch_quant_mxfp8(x, D.T, D.d, s2r, D.k, xq, xs, stream)) != cudaSuccess)
+  if ((e = moe::launch_quant_mxfp8(x, D.T, D.d, s2r, D.k, xq, xs, scale_layout(kernel),
+                                   stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (kernel == MOE_GEMM_WEIGHT_TILES) {
     if ((e = moe::launch_gemm_decode_w13_glu(xq, xs, counts, offsets, D.E, D.d, D.I, W->w13,

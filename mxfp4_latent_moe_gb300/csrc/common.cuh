@@ -74,6 +74,17 @@ __host__ __device__ __forceinline__ int64_t tiled_sf_offset(int64_t r, int64_t b
   return ((r >> 7) * (K >> 7) + (b >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3);
 }
 
+// Byte offset of the scale of row r, 32-block b in the GROUP32 scale layout
+// (activations of the weight-tile GEMMs): one 512-byte block per 32 rows x
+// 128 inputs, row r's four scale codes at bytes (r%32)*16 .. +3, the other
+// twelve bytes of each 16 unused. A tcgen05.cp of the block puts the 32 rows
+// in tensor-memory column 0.
+__host__ __device__ __forceinline__ int64_t group32_sf_offset(int64_t r, int64_t b, int64_t K) {
+  return ((r >> 5) * (K >> 7) + (b >> 2)) * 512 + (r & 31) * 16 + (b & 3);
+}
+
+enum ScaleLayout : int { kScalesTiled128 = 0, kScalesGroup32 = 1 };
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses, mbarriers
 // ---------------------------------------------------------------------------

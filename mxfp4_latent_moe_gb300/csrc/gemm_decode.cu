@@ -14,17 +14,18 @@
 // MXFP4 weights are the A operand (E2M1, kind::mxf8f6f4 format 5), MXFP8
 // activations the B operand (E4M3), one E8M0 scale per 32 inputs each side.
 //
-// Groups are padded to 128 rows (as for gemm.cu) and the per-expert token
-// counts are read on the device: a tile is (expert, weight rows, 128-row chunk
-// of the group) with N = the chunk's tokens rounded up to 32. Every token
-// chunk starts on a 128-row scale atom, so the tokens' scales go to tensor
-// memory with one aligned copy per stage; padding rows past N are never read.
+// Groups are padded to 32 rows and the per-expert token counts are read on
+// the device: a tile is (expert, weight rows, 32-row chunk of the group), MMA
+// N = 32. The activations' scales are in the GROUP32 layout, one 512-byte
+// block per 32 rows x 128 inputs, so a chunk's scales reach tensor-memory
+// column 0 with one aligned copy per stage. A stage is 32 KB of expanded
+// weights + 4 KB of tokens, so five stages fit: 80 KB of weights in flight
+// per SM, the quantity that bounds HBM streaming here.
 //
 // CTA: persistent, one per SM, 320 threads: warp 0 TMA producer, warp 1
 // tensor-memory allocator + single-thread MMA issuer, warps 2-9 epilogue (two
-// per lane quarter, each taking half the tile's tokens); the epilogue copies
-// its accumulator columns to registers and releases tensor memory before the
-// math, so the next tile's MMAs overlap it. The MX block of h is 32
+// per lane quarter, 16 tokens each). Accumulators are double-buffered, so the
+// next tile's MMAs never wait for the epilogue. The MX block of h is 32
 // consecutive features = the 32 lanes of one warp: its amax is one warp
 // reduction per token.
 #include "internal.h"
@@ -35,19 +36,20 @@ namespace {
 
 constexpr int WM = 128;            // weight rows per MMA (M)
 constexpr int BK = 128;            // inputs per stage
-constexpr int NMAX = 128;          // tokens per tile at most
-constexpr int STAGES = 4;
+constexpr int NTOK = 32;           // tokens per tile (MMA N)
+constexpr int STAGES = 5;
 constexpr int kThreads = 320;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAcc1Col = 128;  // second accumulator (up rows / upper w2 rows)
-constexpr uint32_t kSfCol = 256;    // scale slots: 16 columns per stage (A0, A1, B)
+constexpr uint32_t kTmemCols = 256;
+// accumulator buffer b: acc0 at columns [64b, 64b+32), acc1 (up rows / upper
+// w2 rows) at [64b+32, 64b+64); scale slots from column 128, 16 per stage
+constexpr uint32_t kAccStride = 64;
+constexpr uint32_t kAcc1Col = 32;
+constexpr uint32_t kSfCol = 128;
 
 constexpr uint32_t A_TILE = WM * BK;         // one 128-row E2M1 tile in smem (expanded)
 constexpr uint32_t A_TILE_TX = A_TILE / 2;   // its packed bytes (TMA transaction count)
 constexpr uint32_t A_STAGE = 2 * A_TILE;
-constexpr uint32_t B_BOX_ROWS = 32;
-constexpr uint32_t B_BOX = B_BOX_ROWS * BK;  // 4 KB of E4M3 tokens
-constexpr uint32_t B_STAGE = NMAX * BK;
+constexpr uint32_t B_STAGE = NTOK * BK;     // 4 KB of E4M3 tokens
 constexpr uint32_t SF_ATOM = 512;
 
 constexpr uint32_t kOffA = 0;
@@ -55,7 +57,8 @@ constexpr uint32_t kOffB = kOffA + STAGES * A_STAGE;
 constexpr uint32_t kOffSfa = kOffB + STAGES * B_STAGE;
 constexpr uint32_t kOffSfb = kOffSfa + STAGES * 2 * SF_ATOM;
 constexpr uint32_t kOffBars = kOffSfb + STAGES * SF_ATOM;
-constexpr uint32_t kNumBars = 2 * STAGES + 3;  // full[S], empty[S], acc_full, acc_empty, drain
+// full[S], empty[S], acc_full[2], acc_empty[2], drain
+constexpr uint32_t kNumBars = 2 * STAGES + 5;
 constexpr uint32_t kOffMisc = kOffBars + kNumBars * 8;
 constexpr uint32_t kOffSched = kOffMisc + 16;
 constexpr uint32_t kMaxE = 1024;
@@ -64,9 +67,9 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct DecodeParams {
   const uint8_t* a_sf;  // TILED scales of the weights
-  const uint8_t* b_sf;  // TILED scales of the activations
+  const uint8_t* b_sf;  // GROUP32 scales of the activations
   const int* counts;    // [E] tokens per expert
-  const int* offsets;   // [E+1] group offsets (multiples of 128)
+  const int* offsets;   // [E+1] group offsets (multiples of 32)
   int E;
   int K;                // inputs per row
   int I;                // MODE 0: h width; MODE 1: w2 inputs
@@ -79,9 +82,10 @@ struct DecodeParams {
   int* status;
 };
 
+// Tile -> (expert, weight tile, first token row). An expert has
+// ceil(counts[e]/32) token chunks; the chunk index runs fastest.
 __device__ __forceinline__ void decode_tile(int tile, const int* prefix, const int* offs,
-                                            const int* cnts, int E, int& e, int& nt, int& row0,
-                                            int& ntok) {
+                                            const int* cnts, int E, int& e, int& nt, int& row0) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -89,13 +93,10 @@ __device__ __forceinline__ void decode_tile(int tile, const int* prefix, const i
     else hi = mid - 1;
   }
   e = lo;
-  const int cnt = cnts[e];
-  const int chunks = (cnt + NMAX - 1) / NMAX;
+  const int chunks = (cnts[e] + NTOK - 1) / NTOK;
   const int r = tile - prefix[e];
   nt = r / chunks;
-  const int ch = r - nt * chunks;
-  row0 = offs[e] + ch * NMAX;
-  ntok = (min(NMAX, cnt - ch * NMAX) + 31) & ~31;
+  row0 = offs[e] + (r - nt * chunks) * NTOK;
 }
 
 template <int MODE>
@@ -107,9 +108,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
   uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain = acc_empty + 1;
+  uint64_t* acc_full = empty + STAGES;   // [2]
+  uint64_t* acc_empty = acc_full + 2;    // [2]
+  uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* total_holder = reinterpret_cast<int*>(smem + kOffMisc + 8);
@@ -126,8 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 8 * 32);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8 * 32);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -145,11 +148,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
     int s = 0;
-    bool bad = false;  // groups must be multiples of 128 rows holding their counts
+    bool bad = false;  // groups must be multiples of 32 rows holding their counts
     for (int e = e0; e < e1; ++e) {
       const int rows = offs[e + 1] - offs[e];
-      bad |= rows < 0 || rows % NMAX != 0 || cnts[e] < 0 || cnts[e] > rows;
-      s += max(0, (cnts[e] + NMAX - 1) / NMAX) * p.n_tiles;
+      bad |= rows < 0 || rows % NTOK != 0 || cnts[e] < 0 || cnts[e] > rows;
+      s += max(0, (cnts[e] + NTOK - 1) / NTOK) * p.n_tiles;
     }
     bad = __any_sync(0xffffffffu, bad);
     int incl = s;
@@ -161,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = incl - s;
     for (int e = e0; e < e1; ++e) {
       prefix[e] = run;
-      run += max(0, (cnts[e] + NMAX - 1) / NMAX) * p.n_tiles;
+      run += max(0, (cnts[e] + NTOK - 1) / NTOK) * p.n_tiles;
     }
     if (lane == 31) {
       const bool ok = !bad && offs[0] == 0 && int64_t(offs[E]) <= p.rows_capacity;
@@ -183,15 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t filled = 0, last_parity = 0;
       bool failed = false;
       for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
-        int e, nt, row0, ntok;
-        decode_tile(tile, prefix, offs, cnts, E, e, nt, row0, ntok);
+        int e, nt, row0;
+        decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
         // weight rows: MODE 0 gate and up rows, MODE 1 the tile's two 128-row halves
         const int64_t wrow0 = MODE == 0 ? int64_t(e) * 2 * p.I + int64_t(nt) * WM
                                         : int64_t(e) * p.d + int64_t(nt) * 2 * WM;
         const bool two = MODE == 0 || nt * 2 * WM + WM < p.d;
         const int64_t wrow1 = MODE == 0 ? wrow0 + p.I : wrow0 + WM;
-        const uint32_t tx = (two ? 2u : 1u) * (A_TILE_TX + SF_ATOM) +
-                            uint32_t(ntok / int(B_BOX_ROWS)) * B_BOX + SF_ATOM;
+        const uint32_t tx = (two ? 2u : 1u) * (A_TILE_TX + SF_ATOM) + B_STAGE + SF_ATOM;
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             failed = true;
@@ -209,9 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_load(ssfa + SF_ATOM, p.a_sf + ((wrow1 >> 7) * KT + kt) * SF_ATOM, SF_ATOM,
                       &full[stage]);
           }
-          for (int j = 0; j < ntok / int(B_BOX_ROWS); ++j)
-            tma_load_2d(sb + j * B_BOX, &tmap_x, &full[stage], kt * BK, row0 + j * B_BOX_ROWS);
-          bulk_load(ssfb, p.b_sf + (int64_t(row0 >> 7) * KT + kt) * SF_ATOM, SF_ATOM,
+          tma_load_2d(sb, &tmap_x, &full[stage], kt * BK, row0);
+          bulk_load(ssfb, p.b_sf + (int64_t(row0 >> 5) * KT + kt) * SF_ATOM, SF_ATOM,
                     &full[stage]);
           filled |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -234,18 +235,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, WM, NTOK);
+      uint32_t stage = 0, phase = 0;
+      uint32_t acc_phases = 0;  // bit b: phase parity of accumulator buffer b
+      int buf = 0;
       bool failed = false;
       for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
-        int e, nt, row0, ntok;
-        decode_tile(tile, prefix, offs, cnts, E, e, nt, row0, ntok);
+        int e, nt, row0;
+        decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
         const bool two = MODE == 0 || nt * 2 * WM + WM < p.d;
-        const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, WM, ntok);
-        if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag)) {
+        if (!mbar_wait(&acc_empty[buf], ((acc_phases >> buf) & 1u) ^ 1u, abort_flag)) {
           failed = true;
           break;
         }
         tc_fence_after();
+        const uint32_t acc = tmem_base + uint32_t(buf) * kAccStride;
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             failed = true;
@@ -266,10 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 32; ++kk) {
             const uint32_t id = idesc_with_sf_id(idesc, uint32_t(kk));
             const uint32_t accum = (kt > 0 || kk > 0) ? 1u : 0u;
-            tc_mma_mx(tmem_base, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), id, sf_t,
+            tc_mma_mx(acc, adesc + uint64_t(2 * kk), bdesc + uint64_t(2 * kk), id, sf_t,
                       sf_t + 8, accum);
             if (two)
-              tc_mma_mx(tmem_base + kAcc1Col, adesc + uint64_t((A_TILE >> 4) + 2 * kk),
+              tc_mma_mx(acc + kAcc1Col, adesc + uint64_t((A_TILE >> 4) + 2 * kk),
                         bdesc + uint64_t(2 * kk), id, sf_t + 4, sf_t + 8, accum);
           }
           tc_commit(&empty[stage]);
@@ -279,8 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (failed) break;
-        tc_commit(acc_full);
-        acc_phase ^= 1u;
+        tc_commit(&acc_full[buf]);
+        acc_phases ^= 1u << buf;
+        buf ^= 1;
       }
       if (failed) {
         *abort_flag = 1;
@@ -293,15 +298,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     // Thread = one weight row (tensor-memory lane) of the tile; the two warps
-    // of a lane quarter split the tile's tokens in halves of ntok/2 (16..64).
+    // of a lane quarter take tokens [0, 16) and [16, 32) of the chunk.
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
-    uint32_t acc_phase = 0;
+    uint32_t acc_phases = 0;
+    int buf = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      int e, nt, row0, ntok;
-      decode_tile(tile, prefix, offs, cnts, E, e, nt, row0, ntok);
+      int e, nt, row0;
+      decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
       const bool two = MODE == 0 || nt * 2 * WM + WM < p.d;
-      bool ok = mbar_wait(acc_full, acc_phase, abort_flag);
+      bool ok = mbar_wait(&acc_full[buf], (acc_phases >> buf) & 1u, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         *abort_flag = 1;
@@ -309,46 +315,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int hn = ntok >> 1;          // tokens of this warp
-      const int t0 = half * hn;          // first of them
-      const int nch = hn >> 4;           // 16-token chunks (1..4)
-      const uint32_t tq = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(t0);
-      uint32_t v0[4][16], v1[4][16];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c < nch) {
-          tmem_ld_32x32b_x16(tq + 16 * c, v0[c]);
-          if (two) tmem_ld_32x32b_x16(tq + kAcc1Col + 16 * c, v1[c]);
-        }
-      }
+      const uint32_t tq = tmem_base + uint32_t(buf) * kAccStride + (uint32_t(q * 32) << 16) +
+                          uint32_t(16 * half);
+      uint32_t v0[16], v1[16];
+      tmem_ld_32x32b_x16(tq, v0);
+      if (two) tmem_ld_32x32b_x16(tq + kAcc1Col, v1);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(acc_empty);
-      acc_phase ^= 1u;
+      mbar_arrive(&acc_empty[buf]);
+      acc_phases ^= 1u << buf;
+      buf ^= 1;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c >= nch) break;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int64_t row = int64_t(row0) + t0 + 16 * c + i;
-          if (MODE == 0) {
-            const float gf = __uint_as_float(v0[c][i]);
-            const float h = __fdividef(gf * __uint_as_float(v1[c][i]), 1.0f + __expf(-gf));
-            // amax over the warp's 32 features = one MX block of the token's h row
-            const float amax =
-                __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
-            const int code = mx_scale_code(amax);
-            const int feat = nt * WM + q * 32 + lane;
-            p.out_q[row * p.I + feat] = uint8_t(e4m3x2(h * mx_scale_mult(code), 0.0f) & 0xFFu);
-            if (lane == 0) p.out_sf[tiled_sf_offset(row, feat >> 5, p.I)] = uint8_t(code);
-          } else {
-            const int feat = nt * 2 * WM + q * 32 + lane;
-            p.out_bf16[row * p.d + feat] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v0[c][i])));
-            if (two)
-              p.out_bf16[row * p.d + feat + WM] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v1[c][i])));
-          }
+      for (int i = 0; i < 16; ++i) {
+        const int64_t row = int64_t(row0) + 16 * half + i;
+        if (MODE == 0) {
+          const float gf = __uint_as_float(v0[i]);
+          const float h = __fdividef(gf * __uint_as_float(v1[i]), 1.0f + __expf(-gf));
+          // amax over the warp's 32 features = one MX block of the token's h row
+          const float amax =
+              __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
+          const int code = mx_scale_code(amax);
+          const int feat = nt * WM + q * 32 + lane;
+          p.out_q[row * p.I + feat] = uint8_t(e4m3x2(h * mx_scale_mult(code), 0.0f) & 0xFFu);
+          if (lane == 0) p.out_sf[group32_sf_offset(row, feat >> 5, p.I)] = uint8_t(code);
+        } else {
+          const int feat = nt * 2 * WM + q * 32 + lane;
+          p.out_bf16[row * p.d + feat] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v0[i])));
+          if (two)
+            p.out_bf16[row * p.d + feat + WM] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v1[i])));
         }
       }
     }
@@ -369,7 +365,7 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tw, const CU
   if (err != cudaSuccess) return err;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  const int64_t max_tiles = (p.rows_capacity / NMAX) * p.n_tiles;
+  const int64_t max_tiles = (p.rows_capacity / NTOK) * p.n_tiles;
   const int grid = int(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
   grouped_gemm_decode_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(tw, tx, p);
   return cudaGetLastError();
@@ -384,7 +380,7 @@ cudaError_t launch_gemm_decode_w13_glu(const uint8_t* xq, const uint8_t* xs, con
                                        cudaStream_t st) {
   CUtensorMap tw, tx;
   if (!encode_operand(&tw, w13, true, d, int64_t(E) * 2 * I, WM)) return cudaErrorInvalidValue;
-  if (!encode_operand(&tx, xq, false, d, rows_capacity, B_BOX_ROWS)) return cudaErrorInvalidValue;
+  if (!encode_operand(&tx, xq, false, d, rows_capacity, NTOK)) return cudaErrorInvalidValue;
   DecodeParams p{};
   p.a_sf = w13_sf;
   p.b_sf = xs;
@@ -408,7 +404,7 @@ cudaError_t launch_gemm_decode_w2(const uint8_t* hq, const uint8_t* hs, const in
                                   int* status, cudaStream_t st) {
   CUtensorMap tw, tx;
   if (!encode_operand(&tw, w2, true, I, int64_t(E) * d, WM)) return cudaErrorInvalidValue;
-  if (!encode_operand(&tx, hq, false, I, rows_capacity, B_BOX_ROWS)) return cudaErrorInvalidValue;
+  if (!encode_operand(&tx, hq, false, I, rows_capacity, NTOK)) return cudaErrorInvalidValue;
   DecodeParams p{};
   p.a_sf = w2_sf;
   p.b_sf = hs;

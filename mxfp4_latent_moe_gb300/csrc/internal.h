@@ -15,7 +15,7 @@ cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* 
                            int64_t rows_capacity, int* hist, int* status, cudaStream_t st);
 
 cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
-                               uint8_t* codes, uint8_t* scales, cudaStream_t st);
+                               uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st);
 cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                                   cudaStream_t st);
 

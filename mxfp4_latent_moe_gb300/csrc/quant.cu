@@ -30,6 +30,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
   }
 }
 
+template <int LAYOUT>
 __global__ void __launch_bounds__(kQuantThreads)
     quant_mxfp8_kernel(const uint4* __restrict__ x, int d, const int* __restrict__ slot_to_row,
                        int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
@@ -65,8 +66,11 @@ __global__ void __launch_bounds__(kQuantThreads)
   for (int j = 0; j < nrows; ++j) {
     const int64_t row = slot_to_row ? int64_t(__ldg(slot_to_row + t * k + j)) : t;
     *reinterpret_cast<uint2*>(codes + row * d + int64_t(v) * 8) = packed;
-    if ((lane & 15) == 0)
-      *reinterpret_cast<uint32_t*>(scales + tiled_sf_offset(row, int64_t(v >> 2), d)) = sword;
+    if ((lane & 15) == 0) {
+      const int64_t off = LAYOUT == kScalesGroup32 ? group32_sf_offset(row, int64_t(v >> 2), d)
+                                                   : tiled_sf_offset(row, int64_t(v >> 2), d);
+      *reinterpret_cast<uint32_t*>(scales + off) = sword;
+    }
   }
 }
 
@@ -89,12 +93,16 @@ __global__ void prepack_scales_kernel(const uint8_t* __restrict__ src, int64_t r
 }  // namespace
 
 cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
-                               uint8_t* codes, uint8_t* scales, cudaStream_t st) {
+                               uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st) {
   const int64_t total = int64_t(T) * (d / 8);
   if (total == 0 || (slot_to_row && k == 0)) return cudaSuccess;
   const int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
-  quant_mxfp8_kernel<<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
-      reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
+  if (layout == kScalesGroup32)
+    quant_mxfp8_kernel<kScalesGroup32><<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
+  else
+    quant_mxfp8_kernel<kScalesTiled128><<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
   return cudaGetLastError();
 }
 

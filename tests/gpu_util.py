@@ -22,6 +22,24 @@ def tiled_index(rows, K):
     return ((r // 128) * (K // 128) + b // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + b % 4
 
 
+def group32_index(rows, K):
+    """Byte offsets of scale (r, b) in the GROUP32 layout, shape [rows][K/32]."""
+    r = np.arange(rows, dtype=np.int64)[:, None]
+    b = np.arange(K // 32, dtype=np.int64)[None, :]
+    return ((r // 32) * (K // 128) + b // 4) * 512 + (r % 32) * 16 + b % 4
+
+
+def untile_g32(buf, rows, K):
+    return buf.reshape(-1)[group32_index(rows, K)]
+
+
+def tile_g32(canon, K):
+    rows = canon.shape[0]
+    out = np.zeros((rows + 31) // 32 * 32 * K // 8, np.uint8)
+    out[group32_index(rows, K)] = canon
+    return out
+
+
 def untile(tiled, rows, K):
     flat = tiled.reshape(-1)
     return flat[tiled_index(rows, K)]

@@ -45,6 +45,10 @@ def test_size_helpers():
     assert abi.moe_tiled_scale_bytes(1, 3584) == 128 * 112
     assert abi.moe_tiled_scale_bytes(896 * 6144, 3584) == 896 * 6144 * 112
     assert abi.moe_tiled_scale_bytes(10, 100) == 0       # K not a multiple of 128
+    assert abi.moe_activation_scale_bytes(1, 3584, abi.SCALES_TILED128) == 128 * 112
+    assert abi.moe_activation_scale_bytes(1, 3584, abi.SCALES_GROUP32) == 32 * 3584 // 8
+    assert abi.moe_activation_scale_bytes(64, 256, abi.SCALES_GROUP32) == 2 * 512 * 2
+    assert abi.moe_activation_scale_bytes(64, 256, 5) == 0
     # T*k + min(E, T*k)*(pad_m - 1), rounded up to 128
     assert abi.moe_rows_capacity(64, 896, 16, 128) == (1024 + 896 * 127 + 127) // 128 * 128
     assert abi.moe_rows_capacity(8, 32, 4, 128) == (32 + 32 * 127 + 127) // 128 * 128
@@ -80,8 +84,11 @@ def test_host_validation_rejects_before_any_launch(L):
     assert _rc(L, "moe_permute", fake, 4, E, k, 128, fake, fake, fake, fake, 10 ** 6, fake, 16,
                None) == abi.WORKSPACE_TOO_SMALL
     # quant: d not a multiple of 128, misaligned x
-    assert _rc(L, "moe_quant_mxfp8", fake, 4, 100, None, 0, fake, fake, 128, None) == abi.UNSUPPORTED
-    assert _rc(L, "moe_quant_mxfp8", ctypes.c_void_p(4098), 4, 256, None, 0, fake, fake, 128,
+    assert _rc(L, "moe_quant_mxfp8", fake, 4, 100, None, 0, fake, fake, 0, 128, None) == \
+        abi.UNSUPPORTED
+    assert _rc(L, "moe_quant_mxfp8", fake, 4, 256, None, 0, fake, fake, 2, 128, None) == \
+        abi.UNSUPPORTED                                     # unknown scale layout
+    assert _rc(L, "moe_quant_mxfp8", ctypes.c_void_p(4098), 4, 256, None, 0, fake, fake, 1, 128,
                None) == abi.INVALID_ARGUMENT
     # GEMMs: unknown kernel, capacity not a multiple of 128, misaligned weights, no workspace
     args = [fake, fake, fake, fake, E, 3584, 3072]

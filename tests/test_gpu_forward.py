@@ -83,13 +83,16 @@ def _sample_tokens(wl, L, n):
     return np.array(sorted(idx))
 
 
-@pytest.mark.parametrize("name", ["decode_t64", "decode_t512", "prefill_skewed_t8192",
-                                  "prefill_outlier_t32768"])
-def test_forward_full_size_workloads(abi, orc, name):
-    """The benchmark's configuration: kernel family chosen by moe_default_kernel."""
+@pytest.mark.parametrize("name,kernel", [("decode_t64", 0), ("decode_t512", 0),
+                                         ("prefill_skewed_t8192", 0),
+                                         ("prefill_outlier_t32768", 0),
+                                         ("decode_t64", 2), ("decode_t512", 2)])
+def test_forward_full_size_workloads(abi, orc, name, kernel):
+    """The benchmark's configuration (kernel family 0 = moe_default_kernel), and
+    the decode workloads through the weight-tile family."""
     wl = synth.workload(name)
     L = synth.make_layer(wl, seed=0, device="cuda")
-    y, ids, w = _run_forward(abi, wl, L)
+    y, ids, w = _run_forward(abi, wl, L, kernel)
     logits = L["logits"].cpu().numpy()
     # routing: every token
     rids, rw = orc.route_topk(logits, wl.k)

@@ -2,8 +2,9 @@
 oracle's per-expert stage functions, on ragged expert groups: empty groups,
 groups of 1, 15..17, 127..129 and several hundred rows, K not a multiple of the
 pipeline depth, and more tiles than SMs. Both kernel families: token tiles
-(tokens on the MMA's M side) and weight tiles (weights on the M side, an
-expert's tokens as N = its count rounded up to 32, at most 128 per tile)."""
+(tokens on the MMA's M side, groups padded to 128, TILED activation scales)
+and weight tiles (weights on the M side, tokens as N = 32 per tile, groups
+padded to 32, GROUP32 activation scales)."""
 import numpy as np
 import pytest
 import torch
@@ -19,13 +20,22 @@ def abi():
     return gu.cuda_lib()
 
 
-def _groups(sizes):
+def _groups(sizes, kernel):
+    pad = 128 if kernel == 1 else 32
     offsets = [0]
     for c in sizes:
-        offsets.append(offsets[-1] + (c + 127) // 128 * 128)
+        offsets.append(offsets[-1] + (c + pad - 1) // pad * pad)
     rows = [(e, offsets[e] + i) for e, c in enumerate(sizes) for i in range(c)]
     return (np.array(sizes, np.int32), np.array(offsets, np.int32), rows,
-            max(offsets[-1], 128))
+            max((offsets[-1] + 127) // 128 * 128, 128))
+
+
+def _act_scales(canon, K, kernel):
+    return gu.tile(canon, K) if kernel == 1 else gu.tile_g32(canon, K)
+
+
+def _act_untile(buf, rows, K, kernel):
+    return gu.untile(buf, rows, K) if kernel == 1 else gu.untile_g32(buf, rows, K)
 
 
 def _dev(a):
@@ -65,21 +75,23 @@ CASES = [
 @pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("sizes,d,I", CASES)
 def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel):
-    counts, offsets, rows, rc = _groups(sizes)
+    counts, offsets, rows, rc = _groups(sizes, kernel)
     E = len(sizes)
     W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=1)
     xq = synth.random_e4m3_codes((rc, d), seed=2).numpy()
     xs = synth.random_scale_codes((rc, d // 32), lo=118, hi=130, seed=3).numpy()
     hq = torch.zeros(rc, I, dtype=torch.uint8, device="cuda")
-    hs = torch.zeros(abi.moe_tiled_scale_bytes(rc, I), dtype=torch.uint8, device="cuda")
+    hs = torch.zeros(abi.moe_activation_scale_bytes(rc, I, kernel - 1), dtype=torch.uint8,
+                     device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    abi.moe_grouped_gemm_w13_glu(_dev(xq), _dev(gu.tile(xs, d)), _dev(counts), _dev(offsets), E, d,
+    abi.moe_grouped_gemm_w13_glu(_dev(xq), _dev(_act_scales(xs, d, kernel)), _dev(counts),
+                                 _dev(offsets), E, d,
                                  I, kernel,
                                  W["w13"].cuda(), _prepacked(abi, W["w13_s"].numpy(), E * 2 * I, d),
                                  hq, hs, rc, ws)
     assert abi.moe_check_device_status(ws) == 0
     got_c = hq.cpu().numpy()
-    got_s = gu.untile(hs.cpu().numpy(), rc, I)
+    got_s = _act_untile(hs.cpu().numpy(), rc, I, kernel)
     w13, w13s = W["w13"].numpy(), W["w13_s"].numpy()
     idx = [r for _, r in rows]
     ref = np.stack([orc.expert_stage1(xq[r], xs[r], w13[e], w13s[e]) for e, r in rows])
@@ -90,14 +102,15 @@ def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel):
 @pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("sizes,d,I", CASES)
 def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I, kernel):
-    counts, offsets, rows, rc = _groups(sizes)
+    counts, offsets, rows, rc = _groups(sizes, kernel)
     E = len(sizes)
     W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=4)
     hq = synth.random_e4m3_codes((rc, I), seed=5).numpy()
     hs = synth.random_scale_codes((rc, I // 32), lo=118, hi=130, seed=6).numpy()
     yp = torch.zeros(rc, d, dtype=torch.bfloat16, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    abi.moe_grouped_gemm_w2(_dev(hq), _dev(gu.tile(hs, I)), _dev(counts), _dev(offsets), E, I, d,
+    abi.moe_grouped_gemm_w2(_dev(hq), _dev(_act_scales(hs, I, kernel)), _dev(counts),
+                            _dev(offsets), E, I, d,
                             kernel,
                             W["w2"].cuda(), _prepacked(abi, W["w2_s"].numpy(), E * d, I), yp, rc,
                             ws)
@@ -120,7 +133,7 @@ def test_gemm_refuses_bad_groups(abi):
     hq = torch.full((rc, I), 0x5A, dtype=torch.uint8, device="cuda")
     hs = torch.zeros(abi.moe_tiled_scale_bytes(rc, I), dtype=torch.uint8, device="cuda")
     w13_sf = _prepacked(abi, W["w13_s"].numpy(), 2 * 2 * I, d)
-    bad = [(np.array([48, 48], np.int32), np.array([0, 48, 96], np.int32)),     # not padded to 128
+    bad = [(np.array([48, 48], np.int32), np.array([0, 48, 96], np.int32)),     # not padded
            (np.array([130, 0], np.int32), np.array([0, 128, 256], np.int32)),   # count > group
            (np.array([1, 1], np.int32), np.array([0, 128, 384], np.int32))]     # past the capacity
     for counts, offsets in bad:

@@ -100,15 +100,17 @@ def test_permute_flags_bad_ids_on_device(abi):
     assert got["status"] == 6  # MOE_ERR_DEVICE_BAD_INPUT
 
 
-def _quant_gpu(abi, x_bf16, slot_to_row=None, k=0, rows_capacity=None):
+def _quant_gpu(abi, x_bf16, slot_to_row=None, k=0, rows_capacity=None, layout=0):
     T, d = x_bf16.shape
     rc = rows_capacity or (T + 127) // 128 * 128
     codes = torch.zeros(rc, d, dtype=torch.uint8, device="cuda")
-    scales = torch.zeros(abi.moe_tiled_scale_bytes(rc, d), dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(abi.moe_activation_scale_bytes(rc, d, layout), dtype=torch.uint8,
+                         device="cuda")
     s2r = None if slot_to_row is None else torch.from_numpy(slot_to_row).cuda()
-    abi.moe_quant_mxfp8(x_bf16.cuda(), T, d, s2r, k, codes, scales, rc)
+    abi.moe_quant_mxfp8(x_bf16.cuda(), T, d, s2r, k, codes, scales, rc, layout)
     torch.cuda.synchronize()
-    return codes.cpu().numpy(), gu.untile(scales.cpu().numpy(), rc, d)
+    sc = scales.cpu().numpy()
+    return codes.cpu().numpy(), (gu.untile_g32(sc, rc, d) if layout else gu.untile(sc, rc, d))
 
 
 def _special_rows(d):
@@ -126,10 +128,11 @@ def _special_rows(d):
     return torch.from_numpy(rows).to(torch.bfloat16)
 
 
+@pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("T,d", [(300, 3584), (8, 256), (1, 128)])
-def test_quant_dense_bit_exact(abi, orc, T, d):
+def test_quant_dense_bit_exact(abi, orc, T, d, layout):
     x = torch.randn(T, d, generator=torch.Generator().manual_seed(T)).to(torch.bfloat16)
-    codes, scales = _quant_gpu(abi, x)
+    codes, scales = _quant_gpu(abi, x, layout=layout)
     rc, rs = orc.mx_quant_rows_bf16(synth.bf16_bits(x))
     assert np.array_equal(codes[:T], rc)
     assert np.array_equal(scales[:T], rs)
@@ -153,14 +156,15 @@ def test_quant_outlier_rows_keep_codes_and_shift_scales(abi):
     assert np.array_equal(s1[:64].astype(int), s0[:64].astype(int) + 6)
 
 
-def test_quant_scattered_to_grouped_rows(abi, orc):
+@pytest.mark.parametrize("pad,layout", [(128, 0), (32, 1)])
+def test_quant_scattered_to_grouped_rows(abi, orc, pad, layout):
     T, d, E, k = 700, 3584, 896, 16
     rng = np.random.default_rng(8)
     ids, _ = orc.route_topk(rng.normal(0, 1, (T, E)).astype(np.float32), k)
-    perm = orc.permute(ids, E, 128)
-    rc = abi.moe_rows_capacity(T, E, k, 128)
+    perm = orc.permute(ids, E, pad)
+    rc = abi.moe_rows_capacity(T, E, k, pad)
     x = torch.randn(T, d, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
-    codes, scales = _quant_gpu(abi, x, perm["slot_to_row"], k, rc)
+    codes, scales = _quant_gpu(abi, x, perm["slot_to_row"], k, rc, layout)
     ref_c, ref_s = orc.mx_quant_rows_bf16(synth.bf16_bits(x))
     rows = perm["slot_to_row"].reshape(T, k)
     for j in range(k):
