@@ -53,11 +53,17 @@
  *   x, y        bf16 [T][d] row-major.
  *   logits      fp32 [T][E].
  *   topk_ids    int32 [T][k], topk_w fp32 [T][k]; slot s = t*k + j.
- *   Weights     w13 u8 [E][2I][d/2]: rows 0..I-1 gate (w1), I..2I-1 up (w3);
- *               w2 u8 [E][d][I/2]; two E2M1 codes per byte, even element in
- *               the low nibble. Canonical scales are u8 [rows][K/32] (one
- *               E8M0 code per 32 consecutive inputs); the GEMMs take them in
- *               the TILED layout below, made once by moe_prepack_scales.
+ *   Weights     canonical: w13 u8 [E][2I][d/2]: rows 0..I-1 gate (w1),
+ *               I..2I-1 up (w3); w2 u8 [E][d][I/2]; two E2M1 codes per byte,
+ *               even element in the low nibble; scales u8 [rows][K/32] (one
+ *               E8M0 code per 32 consecutive inputs). The GEMMs take the codes
+ *               in the BOXED layout (moe_prepack_weights) and the scales in the
+ *               TILED layout (moe_prepack_scales), both made once at load.
+ *   BOXED code layout of a matrix of R rows x K inputs (R, K multiples of
+ *   128): contiguous 8 KB boxes of 128 rows x 128 inputs (64 bytes per row),
+ *   box (r/128, c/128) at index (r/128)*(K/128) + c/128; the byte of element
+ *   (r, c) is box*8192 + (r%128)*64 + (c%128)/2. Every tensor-memory-access
+ *   load of a weight box is then one contiguous 8 KB read.
  *   Activations xq u8 [rows][d] and hq u8 [rows][I] E4M3 codes; their scales
  *               in the TILED layout.
  *   TILED scale layout of an operand with R rows and K inputs per row (R
@@ -114,9 +120,9 @@ typedef struct {
 } moe_dims;
 
 typedef struct {
-  const uint8_t* w13;    /* [E][2I][d/2] packed E2M1 */
+  const uint8_t* w13;    /* BOXED codes of w13 viewed as [E*2I][d] (moe_prepack_weights) */
   const uint8_t* w13_sf; /* TILED scales of w13 viewed as [E*2I][d] (moe_prepack_scales) */
-  const uint8_t* w2;     /* [E][d][I/2] packed E2M1 */
+  const uint8_t* w2;     /* BOXED codes of w2 viewed as [E*d][I] */
   const uint8_t* w2_sf;  /* TILED scales of w2 viewed as [E*d][I] */
 } moe_weights;
 
@@ -154,6 +160,12 @@ int64_t moe_rows_capacity(int32_t T, int32_t E, int32_t k, int32_t pad_m);
  * overlap; dst 16-byte aligned. */
 moe_status moe_prepack_scales(const uint8_t* src, int64_t rows, int32_t K, uint8_t* dst,
                               cudaStream_t stream);
+
+/* Canonical packed E2M1 codes [rows][K/2] -> BOXED layout (rows*K/2 bytes).
+ * One-time weight preparation; bytes are moved, not changed. rows % 128 == 0;
+ * src 16-byte and dst 32-byte aligned; no overlap. */
+moe_status moe_prepack_weights(const uint8_t* src, int64_t rows, int32_t K, uint8_t* dst,
+                               cudaStream_t stream);
 
 /* Sigmoid top-k routing ("Kimi K3.1 Pro at a glance", Experts row: "896
  * routed (top-16, sigmoid routing)").
@@ -242,7 +254,9 @@ moe_status moe_quant_mxfp8(const uint16_t* x, int32_t T, int32_t d, const int32_
  * or 32 rows): padding rows inside a tile hold unspecified values, later
  * padding rows are left untouched.
  * ws: at least MOE_STATUS_BYTES; the status word records timeouts.
- * xq, hq 16-byte aligned; w13 32-byte aligned; scale arrays 16-byte aligned. */
+ * w13: BOXED codes (moe_prepack_weights of the [E*2I][d] matrix), w13_sf:
+ * TILED scales (moe_prepack_scales). xq, hq 16-byte aligned; w13 32-byte
+ * aligned; scale arrays 16-byte aligned. */
 moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int32_t* counts,
                                     const int32_t* offsets, int32_t E, int32_t d, int32_t I,
                                     int32_t kernel, const uint8_t* w13, const uint8_t* w13_sf,
@@ -252,7 +266,8 @@ moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const 
 /* Stage 2 grouped GEMM (the down projection w2, 3,072 -> 3,584 in the pages'
  * layer): Yp[r] = H[r] . W2[e]^T with MXFP8 H and MXFP4 W2 on tcgen05
  * block-scaled tensor cores, fp32 accumulation, rounded to bf16.
- * yp bf16 [rows_capacity][d], 16-byte aligned; hq, hs, counts, offsets and
+ * yp bf16 [rows_capacity][d], 16-byte aligned; w2 BOXED codes of the
+ * [E*d][I] matrix and w2_sf its TILED scales; hq, hs, counts, offsets and
  * kernel as produced for / by the stage-1 call. */
 moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32_t* counts,
                                const int32_t* offsets, int32_t E, int32_t I, int32_t d,

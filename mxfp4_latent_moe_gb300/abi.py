@@ -47,6 +47,7 @@ _SIGS = {
     "moe_rows_capacity": (_i64, [_i32, _i32, _i32, _i32]),
     "moe_default_kernel": (_i32, [_i32, _i32, _i32]),
     "moe_prepack_scales": (_i32, [_vp, _i64, _i32, _vp, _vp]),
+    "moe_prepack_weights": (_i32, [_vp, _i64, _i32, _vp, _vp]),
     "moe_route_topk": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_permute_workspace_size": (_sz, [_i32, _i32]),
     "moe_permute": (_i32, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp]),
@@ -151,6 +152,10 @@ def moe_workspace_size(T, d, E, k, I):
 
 def moe_prepack_scales(src, rows, K, dst, stream=None):
     _call("moe_prepack_scales", _ptr(src), rows, K, _ptr(dst), _stream(stream))
+
+
+def moe_prepack_weights(src, rows, K, dst, stream=None):
+    _call("moe_prepack_weights", _ptr(src), rows, K, _ptr(dst), _stream(stream))
 
 
 def moe_route_topk(logits, T, E, k, topk_ids, topk_w, stream=None):

@@ -196,6 +196,17 @@ moe_status moe_prepack_scales(const uint8_t* src, int64_t rows, int32_t K, uint8
   return from_cuda(moe::launch_prepack_scales(src, rows, K, dst, stream));
 }
 
+moe_status moe_prepack_weights(const uint8_t* src, int64_t rows, int32_t K, uint8_t* dst,
+                               cudaStream_t stream) {
+  if (rows < 0) return MOE_ERR_INVALID_ARGUMENT;
+  moe_status s = check_width(K);
+  if (s != MOE_OK) return s;
+  if (rows % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  if (!src || !dst || !aligned(src, 16) || !aligned(dst, 32)) return MOE_ERR_INVALID_ARGUMENT;
+  return from_cuda(moe::launch_prepack_weights(src, rows, K, dst, stream));
+}
+
 moe_status moe_route_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_ids,
                           float* topk_w, cudaStream_t stream) {
   moe_status s = check_routing_shape(T, E, k);

@@ -85,6 +85,15 @@ __host__ __device__ __forceinline__ int64_t group32_sf_offset(int64_t r, int64_t
 
 enum ScaleLayout : int { kScalesTiled128 = 0, kScalesGroup32 = 1 };
 
+// BOXED weight layout (moe_prepack_weights): a packed E2M1 matrix of R rows x
+// K inputs stored as contiguous 8 KB boxes of 128 rows x 128 inputs, box
+// (row tile rt, input tile kt) at index rt*(K/128) + kt, rows of 64 bytes
+// inside. Seen by TMA as a 2-D tensor of 64-byte rows; this is the row
+// coordinate of box (rt, kt).
+__host__ __device__ __forceinline__ int32_t boxed_row(int64_t rt, int kt, int KT) {
+  return int32_t((rt * KT + kt) * 128);
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses, mbarriers
 // ---------------------------------------------------------------------------

@@ -204,17 +204,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t u_row = g_row + p.I;
             mbar_arrive_expect_tx(&full[stage], kStageTx);
             tma_load_2d(sa, &tmap_a, &full[stage], kt * BK, row0);
-            tma_load_2d(sb, &tmap_b, &full[stage], kt * BK, int(g_row));
-            tma_load_2d(sb + B_BYTES / 2, &tmap_b, &full[stage], kt * BK, int(u_row));
+            tma_load_2d(sb, &tmap_b, &full[stage], 0, boxed_row(g_row >> 7, kt, KT));
+            tma_load_2d(sb + B_BYTES / 2, &tmap_b, &full[stage], 0, boxed_row(u_row >> 7, kt, KT));
             bulk_load(ssfa, gsfa, SFA_BYTES, &full[stage]);
             bulk_load(ssfb, p.b_sf + ((g_row >> 7) * KT + kt) * 512, 512, &full[stage]);
             bulk_load(ssfb + 512, p.b_sf + ((u_row >> 7) * KT + kt) * 512, 512, &full[stage]);
           } else {
             const int64_t b_row = int64_t(e) * p.d + int64_t(nt) * BN;
             const bool upper = nt * BN + 128 < p.d;
-            mbar_arrive_expect_tx(&full[stage], kStageTx - (upper ? 0u : 512u));
+            mbar_arrive_expect_tx(&full[stage], kStageTx - (upper ? 0u : 512u + B_TX_BYTES / 2));
             tma_load_2d(sa, &tmap_a, &full[stage], kt * BK, row0);
-            tma_load_2d(sb, &tmap_b, &full[stage], kt * BK, int(b_row));
+            tma_load_2d(sb, &tmap_b, &full[stage], 0, boxed_row(b_row >> 7, kt, KT));
+            if (upper)
+              tma_load_2d(sb + B_BYTES / 2, &tmap_b, &full[stage], 0,
+                          boxed_row((b_row >> 7) + 1, kt, KT));
             bulk_load(ssfa, gsfa, SFA_BYTES, &full[stage]);
             bulk_load(ssfb, p.b_sf + ((b_row >> 7) * KT + kt) * 512, 512, &full[stage]);
             if (upper)
@@ -460,6 +463,22 @@ bool encode_operand(CUtensorMap* map, const void* base, bool e2m1, int K, int64_
   return r == CUDA_SUCCESS;
 }
 
+// Weights in the BOXED layout: 64-byte rows (128 E2M1 inputs), one 128-row
+// box per (row tile, input tile), 128-byte swizzle.
+bool encode_boxed_weights(CUtensorMap* map, const void* base, int64_t rows, int K) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {128u, cuuint64_t(rows / 128) * cuuint64_t(K / 128) * 128u};
+  const cuuint64_t strides[1] = {64u};
+  const cuuint32_t box[2] = {128u, 128u};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides,
+         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -473,7 +492,7 @@ cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int*
                                 int64_t rows_capacity, int* status, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!encode_operand(&ta, xq, false, d, rows_capacity, BM)) return cudaErrorInvalidValue;
-  if (!encode_operand(&tb, w13, true, d, int64_t(E) * 2 * I, 128)) return cudaErrorInvalidValue;
+  if (!encode_boxed_weights(&tb, w13, int64_t(E) * 2 * I, d)) return cudaErrorInvalidValue;
   GemmParams p{};
   p.a_sf = xs;
   p.b_sf = w13_sf;
@@ -497,7 +516,7 @@ cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* coun
                            cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!encode_operand(&ta, hq, false, I, rows_capacity, BM)) return cudaErrorInvalidValue;
-  if (!encode_operand(&tb, w2, true, I, int64_t(E) * d, BN)) return cudaErrorInvalidValue;
+  if (!encode_boxed_weights(&tb, w2, int64_t(E) * d, I)) return cudaErrorInvalidValue;
   GemmParams p{};
   p.a_sf = hs;
   p.b_sf = w2_sf;

@@ -204,10 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* ssfa = smem + kOffSfa + stage * 2 * SF_ATOM;
           uint8_t* ssfb = smem + kOffSfb + stage * SF_ATOM;
           mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_2d(sa, &tmap_w, &full[stage], kt * BK, int(wrow0));
+          tma_load_2d(sa, &tmap_w, &full[stage], 0, boxed_row(wrow0 >> 7, kt, KT));
           bulk_load(ssfa, p.a_sf + ((wrow0 >> 7) * KT + kt) * SF_ATOM, SF_ATOM, &full[stage]);
           if (two) {
-            tma_load_2d(sa + A_TILE, &tmap_w, &full[stage], kt * BK, int(wrow1));
+            tma_load_2d(sa + A_TILE, &tmap_w, &full[stage], 0, boxed_row(wrow1 >> 7, kt, KT));
             bulk_load(ssfa + SF_ATOM, p.a_sf + ((wrow1 >> 7) * KT + kt) * SF_ATOM, SF_ATOM,
                       &full[stage]);
           }
@@ -379,7 +379,7 @@ cudaError_t launch_gemm_decode_w13_glu(const uint8_t* xq, const uint8_t* xs, con
                                        uint8_t* hs, int64_t rows_capacity, int* status,
                                        cudaStream_t st) {
   CUtensorMap tw, tx;
-  if (!encode_operand(&tw, w13, true, d, int64_t(E) * 2 * I, WM)) return cudaErrorInvalidValue;
+  if (!encode_boxed_weights(&tw, w13, int64_t(E) * 2 * I, d)) return cudaErrorInvalidValue;
   if (!encode_operand(&tx, xq, false, d, rows_capacity, NTOK)) return cudaErrorInvalidValue;
   DecodeParams p{};
   p.a_sf = w13_sf;
@@ -403,7 +403,7 @@ cudaError_t launch_gemm_decode_w2(const uint8_t* hq, const uint8_t* hs, const in
                                   const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity,
                                   int* status, cudaStream_t st) {
   CUtensorMap tw, tx;
-  if (!encode_operand(&tw, w2, true, I, int64_t(E) * d, WM)) return cudaErrorInvalidValue;
+  if (!encode_boxed_weights(&tw, w2, int64_t(E) * d, I)) return cudaErrorInvalidValue;
   if (!encode_operand(&tx, hq, false, I, rows_capacity, NTOK)) return cudaErrorInvalidValue;
   DecodeParams p{};
   p.a_sf = w2_sf;

@@ -18,6 +18,8 @@ cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_
                                uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st);
 cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                                   cudaStream_t st);
+cudaError_t launch_prepack_weights(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+                                   cudaStream_t st);
 
 cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,
                                 const int* offsets, int E, int d, int I, const uint8_t* w13,
@@ -32,6 +34,7 @@ cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* coun
 // E2M1 operands use TMA's 16U4_ALIGN16B expansion), and the SM count.
 bool encode_operand(CUtensorMap* map, const void* base, bool e2m1, int K, int64_t rows,
                     int box_rows);
+bool encode_boxed_weights(CUtensorMap* map, const void* base, int64_t rows, int K);
 int sm_count();
 
 cudaError_t launch_gemm_decode_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,

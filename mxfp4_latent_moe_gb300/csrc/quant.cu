@@ -90,6 +90,22 @@ __global__ void prepack_scales_kernel(const uint8_t* __restrict__ src, int64_t r
   *reinterpret_cast<uint32_t*>(dst + tiled_sf_offset(r, int64_t(kt) * 4, K)) = w;
 }
 
+// canonical packed E2M1 [rows][K/2] -> BOXED; one thread per 16-byte chunk of
+// the output (a box row is 64 bytes = 4 chunks).
+__global__ void prepack_weights_kernel(const uint4* __restrict__ src, int K,
+                                       uint4* __restrict__ dst, int64_t chunks) {
+  const int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g >= chunks) return;
+  const int KT = K >> 7;
+  const int64_t box = g >> 9;               // 128 rows x 4 chunks per box
+  const int i = int(g >> 2) & 127;          // row inside the box
+  const int j = int(g) & 3;                 // 16-byte chunk inside the row
+  const int64_t rt = box / KT;
+  const int kt = int(box - rt * KT);
+  const int64_t row = rt * 128 + i;
+  dst[g] = __ldg(src + row * (K >> 5) + kt * 4 + j);   // a row holds K/32 chunks
+}
+
 }  // namespace
 
 cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
@@ -113,6 +129,20 @@ cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8
   if (words == 0) return cudaSuccess;
   const int64_t blocks = (words + 255) / 256;
   prepack_scales_kernel<<<dim3(unsigned(blocks)), 256, 0, st>>>(src, rows, K, dst, words);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
+
+namespace moe {
+
+cudaError_t launch_prepack_weights(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
+                                   cudaStream_t st) {
+  const int64_t chunks = rows * (K / 2) / 16;
+  if (chunks == 0) return cudaSuccess;
+  const int64_t blocks = (chunks + 255) / 256;
+  prepack_weights_kernel<<<dim3(unsigned(blocks)), 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(src), K, reinterpret_cast<uint4*>(dst), chunks);
   return cudaGetLastError();
 }
 

@@ -13,14 +13,20 @@ class MoeLayer:
     """Routed experts of one latent-MoE layer.
 
     w13 u8 [E][2I][d/2] (gate rows, then up rows), w13_s u8 [E][2I][d/32],
-    w2 u8 [E][d][I/2], w2_s u8 [E][d][I/32], all CUDA tensors.
+    w2 u8 [E][d][I/2], w2_s u8 [E][d][I/32], all CUDA tensors in the canonical
+    layout; the layer keeps its own prepacked copies (BOXED codes, TILED
+    scales), so the canonical tensors may be freed afterwards.
     """
 
     def __init__(self, w13, w13_s, w2, w2_s, k, kernel=abi.GEMM_AUTO, stream=None):
         E, two_i, half_d = w13.shape
         self.E, self.I, self.d, self.k, self.kernel = E, two_i // 2, half_d * 2, k, kernel
         dev = w13.device
-        self.w13, self.w2 = w13.contiguous(), w2.contiguous()
+        # one-time weight preparation: codes into the BOXED layout, scales TILED
+        self.w13 = torch.empty_like(w13)
+        self.w2 = torch.empty_like(w2)
+        abi.moe_prepack_weights(w13.contiguous(), E * two_i, self.d, self.w13, stream)
+        abi.moe_prepack_weights(w2.contiguous(), E * self.d, self.I, self.w2, stream)
         self.w13_sf = torch.empty(abi.moe_tiled_scale_bytes(E * two_i, self.d), dtype=torch.uint8,
                                   device=dev)
         self.w2_sf = torch.empty(abi.moe_tiled_scale_bytes(E * self.d, self.I), dtype=torch.uint8,

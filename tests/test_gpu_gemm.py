@@ -42,6 +42,12 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
+def _boxed(abi, codes, rows, K):
+    dst = torch.empty(rows * K // 2, dtype=torch.uint8, device="cuda")
+    abi.moe_prepack_weights(_dev(codes.reshape(rows, K // 2)), rows, K, dst)
+    return dst
+
+
 def _prepacked(abi, scales, rows, K):
     dst = torch.empty(abi.moe_tiled_scale_bytes(rows, K), dtype=torch.uint8, device="cuda")
     abi.moe_prepack_scales(_dev(scales.reshape(rows, K // 32)), rows, K, dst)
@@ -87,7 +93,8 @@ def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel):
     abi.moe_grouped_gemm_w13_glu(_dev(xq), _dev(_act_scales(xs, d, kernel)), _dev(counts),
                                  _dev(offsets), E, d,
                                  I, kernel,
-                                 W["w13"].cuda(), _prepacked(abi, W["w13_s"].numpy(), E * 2 * I, d),
+                                 _boxed(abi, W["w13"].numpy(), E * 2 * I, d),
+                                 _prepacked(abi, W["w13_s"].numpy(), E * 2 * I, d),
                                  hq, hs, rc, ws)
     assert abi.moe_check_device_status(ws) == 0
     got_c = hq.cpu().numpy()
@@ -112,7 +119,8 @@ def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I, kernel):
     abi.moe_grouped_gemm_w2(_dev(hq), _dev(_act_scales(hs, I, kernel)), _dev(counts),
                             _dev(offsets), E, I, d,
                             kernel,
-                            W["w2"].cuda(), _prepacked(abi, W["w2_s"].numpy(), E * d, I), yp, rc,
+                            _boxed(abi, W["w2"].numpy(), E * d, I),
+                            _prepacked(abi, W["w2_s"].numpy(), E * d, I), yp, rc,
                             ws)
     assert abi.moe_check_device_status(ws) == 0
     got = gu.bf16_to_f64(yp)
@@ -133,6 +141,7 @@ def test_gemm_refuses_bad_groups(abi):
     hq = torch.full((rc, I), 0x5A, dtype=torch.uint8, device="cuda")
     hs = torch.zeros(abi.moe_tiled_scale_bytes(rc, I), dtype=torch.uint8, device="cuda")
     w13_sf = _prepacked(abi, W["w13_s"].numpy(), 2 * 2 * I, d)
+    w13_boxed = _boxed(abi, W["w13"].numpy(), 2 * 2 * I, d)
     bad = [(np.array([48, 48], np.int32), np.array([0, 48, 96], np.int32)),     # not padded
            (np.array([130, 0], np.int32), np.array([0, 128, 256], np.int32)),   # count > group
            (np.array([1, 1], np.int32), np.array([0, 128, 384], np.int32))]     # past the capacity
@@ -140,6 +149,6 @@ def test_gemm_refuses_bad_groups(abi):
         for kernel in (1, 2):
             ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
             abi.moe_grouped_gemm_w13_glu(xq, xs, _dev(counts), _dev(offsets), 2, d, I, kernel,
-                                         W["w13"].cuda(), w13_sf, hq, hs, rc, ws)
+                                         w13_boxed, w13_sf, hq, hs, rc, ws)
             assert abi.moe_check_device_status(ws) == 6       # MOE_ERR_DEVICE_BAD_INPUT
     assert bool((hq == 0x5A).all())                           # nothing written

@@ -182,6 +182,17 @@ def test_prepack_scales_matches_layout_definition(abi):
         assert np.array_equal(dst.cpu().numpy(), gu.tile(canon, K))
 
 
+def test_prepack_weights_matches_layout_definition(abi):
+    rng = np.random.default_rng(6)
+    for rows, K in ((256, 3584), (384, 256), (128, 128)):
+        canon = rng.integers(0, 256, (rows, K // 2)).astype(np.uint8)
+        dst = torch.full((rows * K // 2,), 0xAB, dtype=torch.uint8, device="cuda")
+        abi.moe_prepack_weights(torch.from_numpy(canon).cuda(), rows, K, dst)
+        # box (r/128, c/128) at index (r/128)*(K/128) + c/128, 64 bytes per box row
+        ref = canon.reshape(rows // 128, 128, K // 128, 64).transpose(0, 2, 1, 3).reshape(-1)
+        assert np.array_equal(dst.cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("T,k,d", [(100, 16, 3584), (33, 4, 256), (5, 0, 128)])
 def test_combine_matches_weighted_sum(abi, T, k, d):
     rng = np.random.default_rng(T)
