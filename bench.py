@@ -50,11 +50,6 @@ def parse():
     return ap.parse_args()
 
 
-def dist_env():
-    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
-        int(os.environ.get("LOCAL_RANK", "0"))
-
-
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -163,7 +158,8 @@ def oracle_seconds(wl, host, threads):
 
 
 def run_reference(args, wl):
-    rank, world, _ = dist_env()
+    from mxfp4_latent_moe_gb300 import replicas
+    rank, world, _ = replicas.dist_env()
     if rank != 0:
         return
     import torch
@@ -210,7 +206,8 @@ def main():
         return run_reference(args, wl)
 
     import torch
-    rank, world, local = dist_env()
+    from mxfp4_latent_moe_gb300 import replicas
+    rank, world, local = replicas.dist_env()
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
@@ -223,7 +220,7 @@ def main():
     from mxfp4_latent_moe_gb300 import abi
     from mxfp4_latent_moe_gb300.layer import MoeLayer
 
-    L = synth.make_layer(wl, seed=args.seed + rank, device=dev)
+    L = synth.make_layer(wl, seed=replicas.replica_seed(args.seed, rank), device=dev)
     kernel_arg = {"auto": abi.GEMM_AUTO, "token": abi.GEMM_TOKEN_TILES,
                   "weight": abi.GEMM_WEIGHT_TILES}[args.gemm_kernel]
     layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k, kernel=kernel_arg)
@@ -267,8 +264,7 @@ def main():
     torch.cuda.synchronize()
 
     # ---- timed region: K moe_forward calls on device-resident inputs
-    if world > 1:
-        torch.distributed.barrier()
+    replicas.barrier()
     torch.cuda.synchronize()
     sampler.mark()
     if flush is None:
@@ -289,11 +285,8 @@ def main():
         torch.cuda.synchronize()
         total_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps))
     sampler.mark()
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-        torch.distributed.barrier()
+    total_ms = replicas.max_over_ranks(total_ms, dev)
+    replicas.barrier()
     launches_per_step = 8
 
     # ---- per-kernel breakdown: the same kernels through the step entry points
@@ -364,11 +357,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     sampler.stop()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = replicas.max_over_ranks(e0.elapsed_time(e1), dev)
 
     peaks, peak_src = load_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -408,7 +397,7 @@ def main():
     if rank == 0:
         line = {
             "metric": METRIC,
-            "value": world * T * args.steps / (total_ms / 1e3),
+            "value": replicas.aggregate_rate(T, world, args.steps, total_ms),
             "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -427,7 +416,8 @@ def main():
             "roofline": roof,
             "kernels_ms": kms,
             "gpu_launches": launches_per_step * args.steps,
-            "e2e": {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+            "e2e": {"value": replicas.aggregate_rate(T, world, args.steps, e2e_ms),
+                    "unit": "tokens/s",
                     "h2d_bytes_per_step": T * d * 2 + T * E * 4,
                     "d2h_bytes_per_step": T * d * 2},
             "cpu_baseline": cpu,
