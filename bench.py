@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_t64")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override: T tokens at the full layer dims, uniform routing")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=0, help="oracle tokens (0 = automatic)")
@@ -125,16 +127,27 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel, workload, src_hash):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel source; None otherwise."""
+# Kernel source files per GEMM family: a committed traffic figure is only used
+# while these files are unchanged since its capture.
+FAMILY_SOURCES = {
+    "token_tiles": ["mxfp4_latent_moe_gb300/csrc/gemm.cu", "mxfp4_latent_moe_gb300/csrc/common.cuh"],
+    "weight_tiles": ["mxfp4_latent_moe_gb300/csrc/gemm_decode.cu",
+                     "mxfp4_latent_moe_gb300/csrc/common.cuh"],
+}
+
+
+def profiled_traffic(kernel, workload, family):
+    """DRAM bytes per launch of `kernel` (GEMM family `family`) from the
+    committed ncu summary, if it was taken on the current kernel source; None
+    otherwise."""
+    src_hash = source_hash(FAMILY_SOURCES[family])
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_hash") != src_hash:
+    if not e or e.get("kernel_family") != family or e.get("source_hash") != src_hash:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -201,7 +214,7 @@ def run_reference(args, wl):
 def main():
     args = parse()
     from mxfp4_latent_moe_gb300 import synth
-    wl = synth.workload(args.workload)
+    wl = synth.workload(args.workload) if args.tokens <= 0 else synth.full_dims(args.tokens)
     if args.impl == "reference":
         return run_reference(args, wl)
 
@@ -367,22 +380,21 @@ def main():
     bound = "hbm" if t_mem >= t_math else "tensor"
     ms_per_step = total_ms / args.steps
     layer_frac = max(t_mem, t_math) / (ms_per_step / 1e3)
-    src_hash = source_hash(["mxfp4_latent_moe_gb300/csrc/gemm.cu",
-                            "mxfp4_latent_moe_gb300/csrc/common.cuh"])
+    family = "weight_tiles" if kernel == abi.GEMM_WEIGHT_TILES else "token_tiles"
     dom = "gemm_w13_glu"
     dom_s = kms[dom] / 1e3
     if bound == "hbm":
         dom_bytes = U * w13_bytes + valid_rows * (d + d // 32) + valid_rows * (I + I // 32)
         roof = {"kernel": dom, "bound": "hbm", "achieved": dom_bytes / dom_s / 1e9,
                 "peak": hbm_peak, "unit": "GB/s", "frac": dom_bytes / dom_s / 1e9 / hbm_peak,
-                "traffic": profiled_traffic(dom, wl.name, src_hash),
+                "traffic": profiled_traffic(dom, wl.name, family),
                 "algorithmic_bytes": dom_bytes, "peak_source": peak_src}
     else:
         dom_flops = 4.0 * T * k * d * I
         roof = {"kernel": dom, "bound": "tensor", "achieved": dom_flops / dom_s / 1e12,
                 "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": dom_flops / dom_s / 1e12 / tensor_peak,
-                "traffic": profiled_traffic(dom, wl.name, src_hash),
+                "traffic": profiled_traffic(dom, wl.name, family),
                 "algorithmic_flops": dom_flops,
                 "peak_source": peak_src + " bf16 x %.1f (fp8 / bf16 nominal ratio)" % FP8_OVER_BF16}
 

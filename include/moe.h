@@ -139,10 +139,12 @@ int32_t moe_abi_version(void);
  * to a multiple of 128). Returns 0 for unsupported K. */
 size_t moe_tiled_scale_bytes(int64_t rows, int32_t K);
 
-/* The GEMM kernels moe_forward uses for MOE_GEMM_AUTO: currently
- * MOE_GEMM_TOKEN_TILES for every shape (on GB300 it streams the weights
- * faster than MOE_GEMM_WEIGHT_TILES even at 64 tokens). Returns -1 for an
- * unsupported shape. */
+/* The GEMM kernels moe_forward uses for MOE_GEMM_AUTO: MOE_GEMM_WEIGHT_TILES
+ * while the experts average at most 28 routed rows (T*k <= 28*E), else
+ * MOE_GEMM_TOKEN_TILES. On GB300 at the full layer dims the weight tiles
+ * stream the weights at ~93% of HBM bandwidth up to T = 1536 tokens, while
+ * the token tiles are bound by their 128-row tensor work below ~2048 tokens
+ * and win above. Returns -1 for an unsupported shape. */
 int32_t moe_default_kernel(int32_t T, int32_t E, int32_t k);
 
 /* Bytes of an activation scale array for `rows` rows of K inputs in the given
@@ -250,9 +252,8 @@ moe_status moe_quant_mxfp8(const uint16_t* x, int32_t T, int32_t d, const int32_
  * holding counts[e] tokens, offsets[0] == 0, offsets[E] <= rows_capacity.
  * Offsets or counts that break this are refused on the device
  * (MOE_ERR_DEVICE_BAD_INPUT in the status word, nothing written).
- * Each family computes the group rows that hold tokens, in whole tiles (128
- * or 32 rows): padding rows inside a tile hold unspecified values, later
- * padding rows are left untouched.
+ * Only rows that hold tokens are written: padding rows of a group (and their
+ * scales) are left untouched.
  * ws: at least MOE_STATUS_BYTES; the status word records timeouts.
  * w13: BOXED codes (moe_prepack_weights of the [E*2I][d] matrix), w13_sf:
  * TILED scales (moe_prepack_scales). xq, hq 16-byte aligned; w13 32-byte
@@ -268,7 +269,8 @@ moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const 
  * block-scaled tensor cores, fp32 accumulation, rounded to bf16.
  * yp bf16 [rows_capacity][d], 16-byte aligned; w2 BOXED codes of the
  * [E*d][I] matrix and w2_sf its TILED scales; hq, hs, counts, offsets and
- * kernel as produced for / by the stage-1 call. */
+ * kernel as produced for / by the stage-1 call. Padding rows of yp are left
+ * untouched. */
 moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32_t* counts,
                                const int32_t* offsets, int32_t E, int32_t I, int32_t d,
                                int32_t kernel, const uint8_t* w2, const uint8_t* w2_sf,

@@ -147,6 +147,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Warp-uniform form of mbar_wait for a converged warp: every lane polls and
+// the warp agrees on the outcome (false if any lane gave up).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, abort, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// One lane of a converged warp (elect.sync). The TMA producer and the MMA
+// issuer keep their warps converged and issue from the elected lane: on
+// sm_103a tcgen05 and mbarrier instructions from a warp whose other lanes are
+// parked at a divergence point issue several times slower.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0u;
+}
+
 // Orders this thread's earlier generic-proxy shared-memory writes before its
 // later async-proxy operations (TMA, tcgen05.cp) on shared memory.
 __device__ __forceinline__ void fence_proxy_async_shared() {

@@ -18,9 +18,12 @@
 //   warp 0      TMA producer: A box 128x128 bytes, B box(es) of E2M1 expanded
 //               by TMA to one byte slot per element (16U4_ALIGN16B), both
 //               128-byte swizzled; the stage's scale atoms by bulk copy.
-//   warp 1      tensor-memory allocator + single-thread MMA issuer: copies the
-//               stage's scale atoms into tensor memory (tcgen05.cp), issues
-//               the 4 MMAs, frees the smem stage with tcgen05.commit.
+//   warp 1      tensor-memory allocator + MMA issuer: copies the stage's scale
+//               atoms into tensor memory (tcgen05.cp), issues the 4 MMAs,
+//               frees the smem stage with tcgen05.commit.
+//   Warps 0 and 1 run their loops converged (all lanes wait, one elected lane
+//   issues); a loop run by one lane with the rest parked issues its tcgen05
+//   and mbarrier instructions several times slower.
 //   warps 2-9   epilogue: tcgen05.ld of the accumulator (one row and half the
 //               columns per thread) straight into registers, release of the
 //               accumulator, then the fused GLU + MX requant (MODE 0) or the
@@ -182,18 +185,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      uint32_t filled = 0, last_parity = 0;  // per-stage bits of the last fill
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        int e, nt, row0;
-        decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
-        bool failed = false;
-        for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-            failed = true;
-            break;
-          }
+    // The whole warp runs the loop (converged); the elected lane issues.
+    const bool leader = elect_one_sync();
+    uint32_t stage = 0, phase = 0;
+    uint32_t filled = 0, last_parity = 0;  // per-stage bits of the last fill
+    bool failed = false;
+    for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
+      int e, nt, row0;
+      decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
+      for (int kt = 0; kt < KT; ++kt) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag)) {
+          failed = true;
+          break;
+        }
+        if (leader) {
           uint8_t* sa = smem + kOffA + stage * A_BYTES;
           uint8_t* sb = smem + kOffB + stage * B_BYTES;
           uint8_t* ssfa = smem + kOffSfa + stage * SFA_BYTES;
@@ -224,44 +229,46 @@ __global__ void __launch_bounds__(kThreads, 1)
               bulk_load(ssfb + 512, p.b_sf + (((b_row >> 7) + 1) * KT + kt) * 512, 512,
                         &full[stage]);
           }
-          filled |= 1u << stage;
-          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
-        if (failed) {
-          *abort_flag = 1;
-          set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
-          break;
+        __syncwarp();
+        filled |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      // drain: every issued copy has landed before the CTA may exit
-      for (int s = 0; s < STAGES; ++s)
-        if ((filled >> s) & 1u)
-          if (!mbar_wait(&full[s], (last_parity >> s) & 1u, nullptr))
-            set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
     }
-    __syncwarp();
+    if (failed && leader) {
+      *abort_flag = 1;
+      set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    // drain: every issued copy has landed before the CTA may exit
+    for (int s = 0; s < STAGES; ++s)
+      if ((filled >> s) & 1u)
+        if (!mbar_wait_warp(&full[s], (last_parity >> s) & 1u, nullptr) && leader)
+          set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_mxf8f6f4(kFmtE4M3, kFmtE2M1, BM, BN);
-      uint32_t stage = 0, phase = 0, acc_phase = 0;
-      bool failed = false;
-      for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
-        if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag)) {
+    // Converged warp; the elected lane issues every tcgen05 instruction (a
+    // commit tracks the operations of the thread that issues it).
+    const bool leader = elect_one_sync();
+    const uint32_t idesc = idesc_mxf8f6f4(kFmtE4M3, kFmtE2M1, BM, BN);
+    uint32_t stage = 0, phase = 0, acc_phase = 0;
+    bool failed = false;
+    for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
+      if (!mbar_wait_warp(acc_empty, acc_phase ^ 1u, abort_flag)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      for (int kt = 0; kt < KT; ++kt) {
+        if (!mbar_wait_warp(&full[stage], phase, abort_flag)) {
           failed = true;
           break;
         }
         tc_fence_after();
-        for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
-            failed = true;
-            break;
-          }
-          tc_fence_after();
+        if (leader) {
           const uint32_t sa = smem_u32(smem + kOffA + stage * A_BYTES);
           const uint32_t sb = smem_u32(smem + kOffB + stage * B_BYTES);
           const uint32_t ssfa = smem_u32(smem + kOffSfa + stage * SFA_BYTES);
@@ -281,24 +288,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (kt > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
-        if (failed) break;
-        tc_commit(acc_full);
-        acc_phase ^= 1u;
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      if (failed) {
-        *abort_flag = 1;
-        set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
-      }
-      // drain: all issued tensor-core work is complete before tensor memory is freed
-      tc_commit(drain);
-      if (!mbar_wait(drain, 0, nullptr)) set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+      if (failed) break;
+      if (leader) tc_commit(acc_full);
+      __syncwarp();
+      acc_phase ^= 1u;
     }
+    if (failed && leader) {
+      *abort_flag = 1;
+      set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    // drain: all issued tensor-core work is complete before tensor memory is freed
+    if (leader) tc_commit(drain);
     __syncwarp();
+    if (!mbar_wait_warp(drain, 0, nullptr) && leader) set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
   } else {
     // ------------------------------------------------------------ epilogue
     // Eight warps, two per tensor-memory lane quarter (a warp may only access
@@ -325,6 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // MODE 0: gate columns [64 half, 64 half + 64) and the matching up
       // columns (+128). MODE 1: output columns [128 half, 128 half + 128).
       const bool active = MODE == 0 || nt * BN + half * 128 < p.d;
+      // rows past the expert's tokens are padding: not stored
+      const bool live = row0 - offs[e] + q * 32 + lane < cnts[e];
       uint32_t v[4][32];
       if (MODE == 0) {
         tmem_ld_32x32b_x32(tq + 64 * half, v[0]);
@@ -362,15 +373,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             o[w].z = e4m3x4(h[16 * w + 8], h[16 * w + 9], h[16 * w + 10], h[16 * w + 11], m);
             o[w].w = e4m3x4(h[16 * w + 12], h[16 * w + 13], h[16 * w + 14], h[16 * w + 15], m);
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.out_q + row * p.I + int64_t(nt) * 128 +
-                                                (2 * half + c) * 32);
-          dst[0] = o[0];
-          dst[1] = o[1];
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out_q + row * p.I + int64_t(nt) * 128 +
+                                                  (2 * half + c) * 32);
+            dst[0] = o[0];
+            dst[1] = o[1];
+          }
           sword |= uint32_t(code) << (8 * c);
         }
-        *reinterpret_cast<uint16_t*>(
-            p.out_sf + tiled_sf_offset(row, int64_t(nt) * 4 + 2 * half, p.I)) = uint16_t(sword);
-      } else if (active) {
+        if (live)
+          *reinterpret_cast<uint16_t*>(
+              p.out_sf + tiled_sf_offset(row, int64_t(nt) * 4 + 2 * half, p.I)) = uint16_t(sword);
+      } else if (active && live) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[16];

@@ -23,8 +23,8 @@
 // per SM, the quantity that bounds HBM streaming here.
 //
 // CTA: persistent, one per SM, 320 threads: warp 0 TMA producer, warp 1
-// tensor-memory allocator + single-thread MMA issuer, warps 2-9 epilogue (two
-// per lane quarter, 16 tokens each). Accumulators are double-buffered, so the
+// tensor-memory allocator + MMA issuer (both warps converged, one elected
+// lane issues), warps 2-9 epilogue (two per lane quarter, 16 tokens each). Accumulators are double-buffered, so the
 // next tile's MMAs never wait for the epilogue. The MX block of h is 32
 // consecutive features = the 32 lanes of one warp: its amax is one warp
 // reduction per token.
@@ -181,24 +181,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      uint32_t filled = 0, last_parity = 0;
-      bool failed = false;
-      for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
-        int e, nt, row0;
-        decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
-        // weight rows: MODE 0 gate and up rows, MODE 1 the tile's two 128-row halves
-        const int64_t wrow0 = MODE == 0 ? int64_t(e) * 2 * p.I + int64_t(nt) * WM
-                                        : int64_t(e) * p.d + int64_t(nt) * 2 * WM;
-        const bool two = MODE == 0 || nt * 2 * WM + WM < p.d;
-        const int64_t wrow1 = MODE == 0 ? wrow0 + p.I : wrow0 + WM;
-        const uint32_t tx = (two ? 2u : 1u) * (A_TILE_TX + SF_ATOM) + B_STAGE + SF_ATOM;
-        for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-            failed = true;
-            break;
-          }
+    const bool leader = elect_one_sync();
+    uint32_t stage = 0, phase = 0;
+    uint32_t filled = 0, last_parity = 0;
+    bool failed = false;
+    for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
+      int e, nt, row0;
+      decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
+      // weight rows: MODE 0 gate and up rows, MODE 1 the tile's two 128-row halves
+      const int64_t wrow0 = MODE == 0 ? int64_t(e) * 2 * p.I + int64_t(nt) * WM
+                                      : int64_t(e) * p.d + int64_t(nt) * 2 * WM;
+      const bool two = MODE == 0 || nt * 2 * WM + WM < p.d;
+      const int64_t wrow1 = MODE == 0 ? wrow0 + p.I : wrow0 + WM;
+      const uint32_t tx = (two ? 2u : 1u) * (A_TILE_TX + SF_ATOM) + B_STAGE + SF_ATOM;
+      for (int kt = 0; kt < KT; ++kt) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag)) {
+          failed = true;
+          break;
+        }
+        if (leader) {
           uint8_t* sa = smem + kOffA + stage * A_STAGE;
           uint8_t* sb = smem + kOffB + stage * B_STAGE;
           uint8_t* ssfa = smem + kOffSfa + stage * 2 * SF_ATOM;
@@ -214,48 +215,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sb, &tmap_x, &full[stage], kt * BK, row0);
           bulk_load(ssfb, p.b_sf + (int64_t(row0 >> 5) * KT + kt) * SF_ATOM, SF_ATOM,
                     &full[stage]);
-          filled |= 1u << stage;
-          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        }
+        __syncwarp();
+        filled |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      if (failed) {
-        *abort_flag = 1;
-        set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
-      }
-      for (int s = 0; s < STAGES; ++s)
-        if ((filled >> s) & 1u)
-          if (!mbar_wait(&full[s], (last_parity >> s) & 1u, nullptr))
-            set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
     }
-    __syncwarp();
+    if (failed && leader) {
+      *abort_flag = 1;
+      set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    for (int s = 0; s < STAGES; ++s)
+      if ((filled >> s) & 1u)
+        if (!mbar_wait_warp(&full[s], (last_parity >> s) & 1u, nullptr) && leader)
+          set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, WM, NTOK);
-      uint32_t stage = 0, phase = 0;
-      uint32_t acc_phases = 0;  // bit b: phase parity of accumulator buffer b
-      int buf = 0;
-      bool failed = false;
-      for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
-        int e, nt, row0;
-        decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
-        const bool two = MODE == 0 || nt * 2 * WM + WM < p.d;
-        if (!mbar_wait(&acc_empty[buf], ((acc_phases >> buf) & 1u) ^ 1u, abort_flag)) {
+    const bool leader = elect_one_sync();
+    const uint32_t idesc = idesc_mxf8f6f4(kFmtE2M1, kFmtE4M3, WM, NTOK);
+    uint32_t stage = 0, phase = 0;
+    uint32_t acc_phases = 0;  // bit b: phase parity of accumulator buffer b
+    int buf = 0;
+    bool failed = false;
+    for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
+      int e, nt, row0;
+      decode_tile(tile, prefix, offs, cnts, E, e, nt, row0);
+      const bool two = MODE == 0 || nt * 2 * WM + WM < p.d;
+      if (!mbar_wait_warp(&acc_empty[buf], ((acc_phases >> buf) & 1u) ^ 1u, abort_flag)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t acc = tmem_base + uint32_t(buf) * kAccStride;
+      for (int kt = 0; kt < KT; ++kt) {
+        if (!mbar_wait_warp(&full[stage], phase, abort_flag)) {
           failed = true;
           break;
         }
         tc_fence_after();
-        const uint32_t acc = tmem_base + uint32_t(buf) * kAccStride;
-        for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
-            failed = true;
-            break;
-          }
-          tc_fence_after();
+        if (leader) {
           const uint32_t sa = smem_u32(smem + kOffA + stage * A_STAGE);
           const uint32_t sb = smem_u32(smem + kOffB + stage * B_STAGE);
           const uint32_t ssfa = smem_u32(smem + kOffSfa + stage * 2 * SF_ATOM);
@@ -277,24 +279,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bdesc + uint64_t(2 * kk), id, sf_t + 4, sf_t + 8, accum);
           }
           tc_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
-        if (failed) break;
-        tc_commit(&acc_full[buf]);
-        acc_phases ^= 1u << buf;
-        buf ^= 1;
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      if (failed) {
-        *abort_flag = 1;
-        set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
-      }
-      tc_commit(drain);
-      if (!mbar_wait(drain, 0, nullptr)) set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+      if (failed) break;
+      if (leader) tc_commit(&acc_full[buf]);
+      __syncwarp();
+      acc_phases ^= 1u << buf;
+      buf ^= 1;
     }
+    if (failed && leader) {
+      *abort_flag = 1;
+      set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
+    }
+    if (leader) tc_commit(drain);
     __syncwarp();
+    if (!mbar_wait_warp(drain, 0, nullptr) && leader) set_status(p.status, MOE_ERR_DEVICE_TIMEOUT);
   } else {
     // ------------------------------------------------------------ epilogue
     // Thread = one weight row (tensor-memory lane) of the tile; the two warps
@@ -325,8 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&acc_empty[buf]);
       acc_phases ^= 1u << buf;
       buf ^= 1;
+      // rows of the chunk past the expert's tokens are padding: not stored
+      const int live = cnts[e] - (row0 - offs[e]) - 16 * half;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
+        if (i >= live) break;
         const int64_t row = int64_t(row0) + 16 * half + i;
         if (MODE == 0) {
           const float gf = __uint_as_float(v0[i]);

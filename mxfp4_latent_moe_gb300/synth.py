@@ -65,6 +65,11 @@ def workload(name_or_index):
     return BY_NAME[name_or_index]
 
 
+def full_dims(T):
+    """T tokens at the full layer dims (d=3584, E=896, k=16, I=3072), N(0,1) logits."""
+    return Workload("uniform_t%d" % T, T=T, d=3584, E=896, k=16, I=3072)
+
+
 def shape(name, T=None, d=None, E=None, k=None, I=None, **kw):
     """A custom workload (test shapes)."""
     return Workload(name, T=T, d=d, E=E, k=k, I=I, **kw)

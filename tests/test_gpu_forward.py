@@ -86,10 +86,12 @@ def _sample_tokens(wl, L, n):
 @pytest.mark.parametrize("name,kernel", [("decode_t64", 0), ("decode_t512", 0),
                                          ("prefill_skewed_t8192", 0),
                                          ("prefill_outlier_t32768", 0),
-                                         ("decode_t64", 2), ("decode_t512", 2)])
+                                         ("decode_t64", 1), ("decode_t512", 1),
+                                         ("decode_t512", 2), ("prefill_skewed_t8192", 2)])
 def test_forward_full_size_workloads(abi, orc, name, kernel):
-    """The benchmark's configuration (kernel family 0 = moe_default_kernel), and
-    the decode workloads through the weight-tile family."""
+    """The benchmark's configuration (kernel family 0 = moe_default_kernel:
+    weight tiles at decode, token tiles at prefill), and each workload through
+    the other family too."""
     wl = synth.workload(name)
     L = synth.make_layer(wl, seed=0, device="cuda")
     y, ids, w = _run_forward(abi, wl, L, kernel)

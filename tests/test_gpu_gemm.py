@@ -86,9 +86,9 @@ def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel):
     W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=1)
     xq = synth.random_e4m3_codes((rc, d), seed=2).numpy()
     xs = synth.random_scale_codes((rc, d // 32), lo=118, hi=130, seed=3).numpy()
-    hq = torch.zeros(rc, I, dtype=torch.uint8, device="cuda")
-    hs = torch.zeros(abi.moe_activation_scale_bytes(rc, I, kernel - 1), dtype=torch.uint8,
-                     device="cuda")
+    hq = torch.full((rc, I), 0x5A, dtype=torch.uint8, device="cuda")
+    hs = torch.full((abi.moe_activation_scale_bytes(rc, I, kernel - 1),), 0x5A,
+                    dtype=torch.uint8, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     abi.moe_grouped_gemm_w13_glu(_dev(xq), _dev(_act_scales(xs, d, kernel)), _dev(counts),
                                  _dev(offsets), E, d,
@@ -104,6 +104,8 @@ def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel):
     ref = np.stack([orc.expert_stage1(xq[r], xs[r], w13[e], w13s[e]) for e, r in rows])
     ref_c, ref_s = orc.mx_quant_rows(ref.astype(np.float32))
     _check_mxfp8_rows(got_c[idx], got_s[idx], ref_c, ref_s)
+    pad_rows = np.setdiff1d(np.arange(rc), idx)      # never written
+    assert np.all(got_c[pad_rows] == 0x5A) and np.all(got_s[pad_rows] == 0x5A)
 
 
 @pytest.mark.parametrize("kernel", [1, 2])
@@ -114,7 +116,7 @@ def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I, kernel):
     W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=4)
     hq = synth.random_e4m3_codes((rc, I), seed=5).numpy()
     hs = synth.random_scale_codes((rc, I // 32), lo=118, hi=130, seed=6).numpy()
-    yp = torch.zeros(rc, d, dtype=torch.bfloat16, device="cuda")
+    yp = torch.full((rc, d), 7.0, dtype=torch.bfloat16, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     abi.moe_grouped_gemm_w2(_dev(hq), _dev(_act_scales(hs, I, kernel)), _dev(counts),
                             _dev(offsets), E, I, d,
@@ -130,6 +132,8 @@ def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I, kernel):
     rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
     err = np.abs(got[idx] - ref)
     assert np.all(err <= np.abs(ref) * 2.0 ** -8 + 1e-5 * rms), float((err / (rms + 1e-30)).max())
+    pad_rows = np.setdiff1d(np.arange(rc), idx)      # never written
+    assert np.all(got[pad_rows] == 7.0)
 
 
 def test_gemm_refuses_bad_groups(abi):
