@@ -47,6 +47,14 @@ def lib():
             "orc_moe_forward": (None, [_u16p, _f32p, _i64, _i32, _i32, _i32, _i32,
                                        _u8p, _u8p, _u8p, _u8p, _u16p, _i32p, _f32p, _f64p, _i32]),
             "orc_expert_bytes": (_i64, [_i32, _i32]),
+            "orc_e2m1_encode_rne_sat": (ctypes.c_uint8, [ctypes.c_double]),
+            "orc_mxfp4_quant_block": (None, [_f32p, _u8p, _u8p]),
+            "orc_mxfp4_quant_rows": (None, [_f32p, _i64, _i64, _u8p, _u8p]),
+            "orc_mxfp4_quant_rows_bf16": (None, [_u16p, _i64, _i64, _u8p, _u8p]),
+            "orc_expert_stage1_a4": (None, [_u8p, _u8p, _i32, _i32, _u8p, _u8p, _f64p]),
+            "orc_moe_forward_a4w4": (None, [_u16p, _f32p, _i64, _i32, _i32, _i32, _i32,
+                                            _u8p, _u8p, _u8p, _u8p, _u16p, _i32p, _f32p,
+                                            _f64p, _i32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -107,6 +115,30 @@ def mx_quant_rows_bf16(x_bits):
     return codes, scales
 
 
+def e2m1_encode(v):
+    return lib().orc_e2m1_encode_rne_sat(float(v))
+
+
+def mxfp4_quant_rows(v):
+    """fp32 [rows][K] -> (packed E2M1 u8 [rows][K/2], scales u8 [rows][K/32])."""
+    v = _c(v, np.float32)
+    rows, K = v.shape
+    packed = np.empty((rows, K // 2), np.uint8)
+    scales = np.empty((rows, K // 32), np.uint8)
+    lib().orc_mxfp4_quant_rows(_p(v, _f32p), rows, K, _p(packed, _u8p), _p(scales, _u8p))
+    return packed, scales
+
+
+def mxfp4_quant_rows_bf16(x_bits):
+    """bf16 bit patterns (uint16) [rows][K] -> (packed E2M1 [rows][K/2], scales)."""
+    x = _c(x_bits, np.uint16)
+    rows, K = x.shape
+    packed = np.empty((rows, K // 2), np.uint8)
+    scales = np.empty((rows, K // 32), np.uint8)
+    lib().orc_mxfp4_quant_rows_bf16(_p(x, _u16p), rows, K, _p(packed, _u8p), _p(scales, _u8p))
+    return packed, scales
+
+
 def route_topk(logits, k):
     lg = _c(logits, np.float32)
     T, E = lg.shape
@@ -144,6 +176,18 @@ def expert_stage1(xq, xs, w13_e, w13s_e):
     return h
 
 
+def expert_stage1_a4(xq, xs, w13_e, w13s_e):
+    """Stage 1 with an MXFP4 activation row: xq packed E2M1 [d/2], xs [d/32]."""
+    xq, xs = _c(xq, np.uint8), _c(xs, np.uint8)
+    w13_e, w13s_e = _c(w13_e, np.uint8), _c(w13s_e, np.uint8)
+    d = xq.shape[0] * 2
+    I = w13_e.shape[0] // 2
+    h = np.empty(I, np.float64)
+    lib().orc_expert_stage1_a4(_p(xq, _u8p), _p(xs, _u8p), d, I, _p(w13_e, _u8p),
+                               _p(w13s_e, _u8p), _p(h, _f64p))
+    return h
+
+
 def expert_stage2(hq, hs, w2_e, w2s_e):
     hq, hs = _c(hq, np.uint8), _c(hs, np.uint8)
     w2_e, w2s_e = _c(w2_e, np.uint8), _c(w2s_e, np.uint8)
@@ -155,8 +199,10 @@ def expert_stage2(hq, hs, w2_e, w2s_e):
     return y
 
 
-def moe_forward(x_bits, logits, k, w13, w13s, w2, w2s, threads=0, want_y64=False):
+def moe_forward(x_bits, logits, k, w13, w13s, w2, w2s, threads=0, want_y64=False,
+                a4w4=False):
     """Whole layer for independent tokens. x_bits bf16 patterns [n][d].
+    a4w4: MXFP4 stage-1 activations (orc_moe_forward_a4w4).
 
     Returns dict(y=bf16 bits [n][d], ids, w, y64 (or None)).
     """
@@ -170,9 +216,10 @@ def moe_forward(x_bits, logits, k, w13, w13s, w2, w2s, threads=0, want_y64=False
     ids = np.empty((n, max(k, 1)), np.int32)
     w = np.empty((n, max(k, 1)), np.float32)
     y64 = np.empty((n, d), np.float64) if want_y64 else None
-    lib().orc_moe_forward(_p(x, _u16p), _p(lg, _f32p), n, d, E, k, I, _p(w13, _u8p),
-                          _p(w13s, _u8p), _p(w2, _u8p), _p(w2s, _u8p), _p(y, _u16p),
-                          _p(ids, _i32p), _p(w, _f32p), _p(y64, _f64p), threads)
+    fn = lib().orc_moe_forward_a4w4 if a4w4 else lib().orc_moe_forward
+    fn(_p(x, _u16p), _p(lg, _f32p), n, d, E, k, I, _p(w13, _u8p), _p(w13s, _u8p),
+       _p(w2, _u8p), _p(w2s, _u8p), _p(y, _u16p), _p(ids, _i32p), _p(w, _f32p), _p(y64, _f64p),
+       threads)
     return dict(y=y, ids=ids[:, :k], w=w[:, :k], y64=y64)
 
 

@@ -68,6 +68,19 @@ const Tables& tables() {
 
 constexpr double kE4M3Max = 448.0;   // largest finite E4M3 magnitude (code 0x7E)
 constexpr int kE4M3Emax = 8;         // exponent of the largest E4M3 power of two
+constexpr double kE2M1Max = 6.0;     // largest E2M1 magnitude (code 0x7)
+constexpr int kE2M1Emax = 2;         // exponent of the largest E2M1 power of two
+
+// MX shared-exponent scale code for a block whose largest magnitude is amax
+// and whose element format has largest power of two 2^emax (OCP MX v1.0):
+// clamp(floor(log2(amax)) - emax + 127, 0, 254); 0 for an all-zero block.
+int mx_scale_code_for(double amax, int emax) {
+  if (!(amax > 0.0)) return 0;
+  int ex = 0;
+  std::frexp(amax, &ex);             // amax = m * 2^ex, m in [0.5, 1)
+  const int code = (ex - 1) - emax + 127;
+  return std::min(254, std::max(0, code));
+}
 
 float bf16_bits_to_float(uint16_t b) {
   uint32_t u = uint32_t(b) << 16;
@@ -122,14 +135,7 @@ uint8_t orc_e4m3_encode_rne_sat(double v) {
 void orc_mx_quant_block(const float* v32, uint8_t* codes32, uint8_t* scale) {
   double amax = 0.0;
   for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(double(v32[i])));
-  int code = 0;
-  if (amax > 0.0) {
-    int ex = 0;
-    std::frexp(amax, &ex);             // amax = m * 2^ex, m in [0.5, 1)
-    const int floor_log2 = ex - 1;
-    code = floor_log2 - kE4M3Emax + 127;
-    code = std::min(254, std::max(0, code));
-  }
+  const int code = mx_scale_code_for(amax, kE4M3Emax);
   const double X = std::ldexp(1.0, code - 127);
   for (int i = 0; i < 32; ++i) codes32[i] = orc_e4m3_encode_rne_sat(double(v32[i]) / X);
   *scale = uint8_t(code);
@@ -148,6 +154,57 @@ void orc_mx_quant_rows_bf16(const uint16_t* x, int64_t rows, int64_t K, uint8_t*
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t c = 0; c < K; ++c) buf[size_t(c)] = bf16_bits_to_float(x[r * K + c]);
     orc_mx_quant_rows(buf.data(), 1, K, codes + r * K, scales + r * (K / 32));
+  }
+}
+
+// Nearest E2M1 value by search over the non-negative codes 0..7 (their values
+// increase with the code), ties to the even code, magnitudes above 6 saturate
+// to 6. The sign bit follows the sign of v, also for 0.
+uint8_t orc_e2m1_encode_rne_sat(double v) {
+  const Tables& t = tables();
+  const uint8_t sign = std::signbit(v) ? 0x8 : 0x0;
+  const double a = std::fabs(v);
+  if (a >= kE2M1Max) return sign | 0x7;
+  unsigned lo = 0;
+  while (lo + 1 <= 7 && t.e2m1[lo + 1] <= a) ++lo;
+  if (t.e2m1[lo] == a) return sign | uint8_t(lo);
+  const unsigned hi = lo + 1;  // a < 6 so hi <= 7
+  const double dlo = a - t.e2m1[lo], dhi = t.e2m1[hi] - a;
+  unsigned pick;
+  if (dlo < dhi) pick = lo;
+  else if (dhi < dlo) pick = hi;
+  else pick = (lo % 2 == 0) ? lo : hi;
+  return sign | uint8_t(pick);
+}
+
+// The MX rule with E2M1 elements: shared exponent floor(log2(amax)) - 2.
+void orc_mxfp4_quant_block(const float* v32, uint8_t* packed16, uint8_t* scale) {
+  double amax = 0.0;
+  for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(double(v32[i])));
+  const int code = mx_scale_code_for(amax, kE2M1Emax);
+  const double X = std::ldexp(1.0, code - 127);
+  for (int i = 0; i < 16; ++i) {
+    const uint8_t lo = orc_e2m1_encode_rne_sat(double(v32[2 * i]) / X);
+    const uint8_t hi = orc_e2m1_encode_rne_sat(double(v32[2 * i + 1]) / X);
+    packed16[i] = uint8_t(lo | (hi << 4));
+  }
+  *scale = uint8_t(code);
+}
+
+void orc_mxfp4_quant_rows(const float* v, int64_t rows, int64_t K, uint8_t* packed,
+                          uint8_t* scales) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < K / 32; ++b)
+      orc_mxfp4_quant_block(v + r * K + b * 32, packed + r * (K / 2) + b * 16,
+                            scales + r * (K / 32) + b);
+}
+
+void orc_mxfp4_quant_rows_bf16(const uint16_t* x, int64_t rows, int64_t K, uint8_t* packed,
+                               uint8_t* scales) {
+  std::vector<float> buf(static_cast<size_t>(K));
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t c = 0; c < K; ++c) buf[size_t(c)] = bf16_bits_to_float(x[r * K + c]);
+    orc_mxfp4_quant_rows(buf.data(), 1, K, packed + r * (K / 2), scales + r * (K / 32));
   }
 }
 
@@ -214,11 +271,8 @@ int32_t orc_permute(const int32_t* ids, int64_t T, int32_t E, int32_t k, int32_t
 
 // Gate/up projection and GLU of one expert ("3,584->2x3,072" in the page's
 // expert row; SwiGLU stand-in for the undefined SiTU-GLU).
-void orc_expert_stage1(const uint8_t* xq, const uint8_t* xs, int32_t d, int32_t I,
-                       const uint8_t* w13_e, const uint8_t* w13s_e, double* h) {
-  const Tables& t = tables();
-  std::vector<double> xd(static_cast<size_t>(d));
-  for (int32_t c = 0; c < d; ++c) xd[size_t(c)] = t.e4m3[xq[c]] * t.e8m0[xs[c / 32]];
+static void expert_stage1_dequantised(const std::vector<double>& xd, int32_t d, int32_t I,
+                                      const uint8_t* w13_e, const uint8_t* w13s_e, double* h) {
   for (int32_t i = 0; i < I; ++i) {
     double g = 0.0, u = 0.0;
     for (int32_t c = 0; c < d; ++c) {
@@ -227,6 +281,22 @@ void orc_expert_stage1(const uint8_t* xq, const uint8_t* xs, int32_t d, int32_t 
     }
     h[i] = g * sigmoid(g) * u;
   }
+}
+
+void orc_expert_stage1(const uint8_t* xq, const uint8_t* xs, int32_t d, int32_t I,
+                       const uint8_t* w13_e, const uint8_t* w13s_e, double* h) {
+  const Tables& t = tables();
+  std::vector<double> xd(static_cast<size_t>(d));
+  for (int32_t c = 0; c < d; ++c) xd[size_t(c)] = t.e4m3[xq[c]] * t.e8m0[xs[c / 32]];
+  expert_stage1_dequantised(xd, d, I, w13_e, w13s_e, h);
+}
+
+// The same with MXFP4 activations (the A4W4 stage 1).
+void orc_expert_stage1_a4(const uint8_t* xq, const uint8_t* xs, int32_t d, int32_t I,
+                          const uint8_t* w13_e, const uint8_t* w13s_e, double* h) {
+  std::vector<double> xd(static_cast<size_t>(d));
+  for (int32_t c = 0; c < d; ++c) xd[size_t(c)] = weight_value(xq, xs, d, 0, c);
+  expert_stage1_dequantised(xd, d, I, w13_e, w13s_e, h);
 }
 
 // Down projection of one expert ("3,072->3,584"; the FP8 second stage takes
@@ -263,11 +333,11 @@ uint16_t orc_bf16_rne(double v) {
   return sign | uint16_t(u >> 16);
 }
 
-void orc_moe_forward(const uint16_t* x, const float* logits, int64_t n, int32_t d,
-                     int32_t E, int32_t k, int32_t I, const uint8_t* w13,
-                     const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s,
-                     uint16_t* y, int32_t* ids_out, float* w_out, double* y64,
-                     int32_t threads) {
+static void moe_forward_impl(bool act_fp4, const uint16_t* x, const float* logits, int64_t n,
+                             int32_t d, int32_t E, int32_t k, int32_t I, const uint8_t* w13,
+                             const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s,
+                             uint16_t* y, int32_t* ids_out, float* w_out, double* y64,
+                             int32_t threads) {
   const int64_t w13_stride = int64_t(2) * I * (d / 2), w13s_stride = int64_t(2) * I * (d / 32);
   const int64_t w2_stride = int64_t(d) * (I / 2), w2s_stride = int64_t(d) * (I / 32);
 
@@ -276,13 +346,18 @@ void orc_moe_forward(const uint16_t* x, const float* logits, int64_t n, int32_t 
                        std::vector<uint8_t>& hq, std::vector<uint8_t>& hs,
                        std::vector<double>& ye, std::vector<double>& acc,
                        std::vector<int32_t>& ids, std::vector<float>& w) {
-    orc_mx_quant_rows_bf16(x + t * d, 1, d, xq.data(), xs.data());
+    if (act_fp4) orc_mxfp4_quant_rows_bf16(x + t * d, 1, d, xq.data(), xs.data());
+    else orc_mx_quant_rows_bf16(x + t * d, 1, d, xq.data(), xs.data());
     orc_route_topk(logits + t * E, 1, E, k, ids.data(), w.data());
     std::fill(acc.begin(), acc.end(), 0.0);
     for (int32_t j = 0; j < k; ++j) {
       const int64_t e = ids[size_t(j)];
-      orc_expert_stage1(xq.data(), xs.data(), d, I, w13 + e * w13_stride, w13s + e * w13s_stride,
-                        h.data());
+      if (act_fp4)
+        orc_expert_stage1_a4(xq.data(), xs.data(), d, I, w13 + e * w13_stride,
+                             w13s + e * w13s_stride, h.data());
+      else
+        orc_expert_stage1(xq.data(), xs.data(), d, I, w13 + e * w13_stride,
+                          w13s + e * w13s_stride, h.data());
       for (int32_t i = 0; i < I; ++i) h32[size_t(i)] = float(h[size_t(i)]);
       orc_mx_quant_rows(h32.data(), 1, I, hq.data(), hs.data());
       orc_expert_stage2(hq.data(), hs.data(), I, d, w2 + e * w2_stride, w2s + e * w2s_stride,
@@ -314,6 +389,23 @@ void orc_moe_forward(const uint16_t* x, const float* logits, int64_t n, int32_t 
     });
   }
   for (auto& th : pool) th.join();
+}
+
+void orc_moe_forward(const uint16_t* x, const float* logits, int64_t n, int32_t d, int32_t E,
+                     int32_t k, int32_t I, const uint8_t* w13, const uint8_t* w13s,
+                     const uint8_t* w2, const uint8_t* w2s, uint16_t* y, int32_t* ids_out,
+                     float* w_out, double* y64, int32_t threads) {
+  moe_forward_impl(false, x, logits, n, d, E, k, I, w13, w13s, w2, w2s, y, ids_out, w_out, y64,
+                   threads);
+}
+
+void orc_moe_forward_a4w4(const uint16_t* x, const float* logits, int64_t n, int32_t d,
+                          int32_t E, int32_t k, int32_t I, const uint8_t* w13,
+                          const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s,
+                          uint16_t* y, int32_t* ids_out, float* w_out, double* y64,
+                          int32_t threads) {
+  moe_forward_impl(true, x, logits, n, d, E, k, I, w13, w13s, w2, w2s, y, ids_out, w_out, y64,
+                   threads);
 }
 
 int64_t orc_expert_bytes(int32_t d, int32_t I) {

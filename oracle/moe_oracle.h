@@ -99,6 +99,44 @@ void orc_expert_stage1(const uint8_t* xq, const uint8_t* xs, int32_t d, int32_t 
 void orc_expert_stage2(const uint8_t* hq, const uint8_t* hs, int32_t I, int32_t d,
                        const uint8_t* w2_e, const uint8_t* w2s_e, double* y);
 
+/* ---- A4W4 stage 1 (MXFP4 activations) -------------------------------------
+ * The pages' stage-1 kernel is selected by an environment switch named A4W4
+ * ("Appendix: environment variables" of "Kimi K3.1 Pro on AMD Instinct GPUs",
+ * next to the FP8 second-stage switch): 4-bit activations and 4-bit weights.
+ * Reading: the stage-1 activations are MXFP4 (E2M1 elements, one E8M0 scale
+ * per 32, shared exponent floor(log2(amax)) - 2, the OCP MX rule with emax of
+ * E2M1 = 2), elements rounded to nearest-even with saturation to +-6; stage 2
+ * stays MXFP8. */
+
+/* Round-to-nearest-even of a real number to E2M1 with saturation to +-6. The
+ * sign is kept for zero results (code 0x8 for -0). Input must not be NaN. */
+uint8_t orc_e2m1_encode_rne_sat(double v);
+
+/* The MX rule for MXFP4 on one block of 32 fp32 values -> 16 bytes of packed
+ * E2M1 codes (even element in the low nibble) and one E8M0 scale code. */
+void orc_mxfp4_quant_block(const float* v32, uint8_t* packed16, uint8_t* scale);
+
+/* MXFP4 over a row-major [rows][K] matrix of fp32 values or of bf16 bit
+ * patterns: packed codes [rows][K/2], scales [rows][K/32]. */
+void orc_mxfp4_quant_rows(const float* v, int64_t rows, int64_t K,
+                          uint8_t* packed, uint8_t* scales);
+void orc_mxfp4_quant_rows_bf16(const uint16_t* x, int64_t rows, int64_t K,
+                               uint8_t* packed, uint8_t* scales);
+
+/* Stage 1 of one expert on one MXFP4 activation row, in fp64: as
+ * orc_expert_stage1 with xq [d/2] packed E2M1 codes and xs [d/32]. */
+void orc_expert_stage1_a4(const uint8_t* xq, const uint8_t* xs, int32_t d, int32_t I,
+                          const uint8_t* w13_e, const uint8_t* w13s_e, double* h);
+
+/* The whole layer with MXFP4 stage-1 activations (same arguments and
+ * outputs as orc_moe_forward). */
+void orc_moe_forward_a4w4(const uint16_t* x, const float* logits, int64_t n,
+                          int32_t d, int32_t E, int32_t k, int32_t I,
+                          const uint8_t* w13, const uint8_t* w13s,
+                          const uint8_t* w2, const uint8_t* w2s,
+                          uint16_t* y, int32_t* ids, float* w, double* y64,
+                          int32_t threads);
+
 /* Round a real number to the nearest bf16 (ties to even), returning its bits. */
 uint16_t orc_bf16_rne(double v);
 

@@ -63,3 +63,43 @@ def quant_mxfp8(v):
 def bf16_bits_to_f64(bits):
     b = np.asarray(bits, np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+def e2m1_rne_sat(v):
+    """Round to E2M1 by arithmetic, independent of any table search: below 1
+    the step is 0.5 (subnormals), in [2^e, 2^(e+1)) it is 2^(e-1); v/step is
+    rounded half-to-even by numpy (an even multiple of the step is an even
+    code), then magnitudes above 6 saturate. Returns fp64 values, sign kept."""
+    v = np.asarray(v, np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)                       # a = m * 2^ex, m in [0.5, 1)
+    e = np.maximum(ex - 1, 0)                 # exponent of the binade, 0 for a < 1
+    step = np.ldexp(1.0, e - 1)
+    q = np.minimum(np.round(a / step) * step, 6.0)
+    return np.copysign(q, v)
+
+
+def e2m1_code_of(vals):
+    """E2M1 codes of exactly representable values (sign of zero kept), by
+    lookup in the OCP value list."""
+    vals = np.asarray(vals, np.float64)
+    table = e2m1_table()[:8]
+    mag = np.abs(vals)
+    idx = np.array([int(np.flatnonzero(table == m)[0]) for m in mag.reshape(-1)]).reshape(mag.shape)
+    return (idx | (np.signbit(vals).astype(np.int64) << 3)).astype(np.uint8)
+
+
+def quant_mxfp4(v):
+    """fp32 [rows][K] -> (packed E2M1 [rows][K/2], scales) by the OCP MX rule
+    with E2M1 elements (shared exponent floor(log2 amax) - 2), saturation to 6."""
+    v = np.asarray(v, np.float32)
+    rows, K = v.shape
+    b = v.astype(np.float64).reshape(rows, K // 32, 32)
+    amax = np.abs(b).max(axis=2)
+    _, ex = np.frexp(amax)
+    sc = np.clip(ex - 1 - 2 + 127, 0, 254)
+    sc[amax == 0] = 0
+    q = e2m1_rne_sat(b / np.ldexp(1.0, sc - 127)[:, :, None])
+    codes = e2m1_code_of(q).reshape(rows, K)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, sc.astype(np.uint8)
