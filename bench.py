@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s and % roofline (HBM GB/s decode, tensor TFLOP/s prefill), 1xGB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense ratio: kind::mxf8f6f4 runs at the FP8 rate
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio: kind::mxf4 (A4W4 stage 1) runs at the FP4 rate
 
 
 def parse():
@@ -49,6 +50,8 @@ def parse():
     ap.add_argument("--cpu-sample", type=int, default=0, help="oracle tokens (0 = automatic)")
     ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "token", "weight"],
                     help="grouped-GEMM family (auto = the library's default for the shape)")
+    ap.add_argument("--a4w4", action="store_true",
+                    help="MXFP4 stage-1 activations (moe_forward_a4w4); the family is stage 2's")
     return ap.parse_args()
 
 
@@ -161,12 +164,12 @@ def oracle_inputs(L, n_tokens):
     return xb, lg, W
 
 
-def oracle_seconds(wl, host, threads):
+def oracle_seconds(wl, host, threads, a4w4=False):
     """Time the CPU oracle, as it stands, on the prepared token sample."""
     import oracle
     xb, lg, W = host
     t0 = time.perf_counter()
-    oracle.moe_forward(xb, lg, wl.k, *W, threads=threads)
+    oracle.moe_forward(xb, lg, wl.k, *W, threads=threads, a4w4=a4w4)
     return time.perf_counter() - t0
 
 
@@ -186,13 +189,13 @@ def run_reference(args, wl):
         n = args.cpu_sample
     else:  # size the per-step sample so the whole run takes about 150 s
         n0 = min(wl.T, cores)
-        per_token = oracle_seconds(wl, oracle_inputs(L, n0), cores) / n0
+        per_token = oracle_seconds(wl, oracle_inputs(L, n0), cores, args.a4w4) / n0
         n = max(1, min(wl.T, int(150.0 / (args.steps + args.warmup) / per_token)))
     host = oracle_inputs(L, n)
     del L
     times = []
     for i in range(args.warmup + args.steps):
-        dt = oracle_seconds(wl, host, cores)
+        dt = oracle_seconds(wl, host, cores, args.a4w4)
         if i >= args.warmup:
             times.append(dt)
     total = sum(times)
@@ -202,7 +205,8 @@ def run_reference(args, wl):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000 * total / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I},
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I,
+                   "a4w4": bool(args.a4w4)},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": "first %d tokens of the workload per step, full layer" % n},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -246,7 +250,7 @@ def main():
     stream = torch.cuda.current_stream()
 
     def fwd():
-        layer.forward(x, logits, ws=ws, y=y, topk_ids=ids, topk_w=w)
+        layer.forward(x, logits, ws=ws, y=y, topk_ids=ids, topk_w=w, a4w4=args.a4w4)
 
     # routing statistics for the roofline (outside any timed region)
     fwd()
@@ -255,9 +259,10 @@ def main():
     counts = torch.bincount(ids.reshape(-1).long(), minlength=E)
     U = int((counts > 0).sum())
     valid_rows = T * k
-    kernel = layer.kernel_for(T)
-    pad = 32 if kernel == abi.GEMM_WEIGHT_TILES else 128
+    kernel = layer.kernel_for(T)      # both stages, or stage 2 under --a4w4
+    pad = 32 if kernel == abi.GEMM_WEIGHT_TILES and not args.a4w4 else 128
     layout = abi.SCALES_GROUP32 if kernel == abi.GEMM_WEIGHT_TILES else abi.SCALES_TILED128
+    xs_layout = abi.SCALES_TILED128 if args.a4w4 else layout
     rows_cap = abi.moe_rows_capacity(T, E, k, pad)
     padded_rows = int(((counts + pad - 1) // pad * pad).sum())
     expert_bytes = layer.weight_bytes_per_expert()
@@ -309,19 +314,29 @@ def main():
     s2r = torch.empty(T * k, dtype=torch.int32, device=dev)
     r2s = torch.empty(rc, dtype=torch.int32, device=dev)
     pws = torch.zeros(abi.moe_permute_workspace_size(T, E), dtype=torch.uint8, device=dev)
-    xq = torch.empty(rc, d, dtype=torch.uint8, device=dev)
-    xs = torch.empty(abi.moe_activation_scale_bytes(rc, d, layout), dtype=torch.uint8, device=dev)
+    xq = torch.empty(rc, d // 2 if args.a4w4 else d, dtype=torch.uint8, device=dev)
+    xs = torch.empty(abi.moe_activation_scale_bytes(rc, d, xs_layout), dtype=torch.uint8,
+                     device=dev)
     hq = torch.empty(rc, I, dtype=torch.uint8, device=dev)
     hs = torch.empty(abi.moe_activation_scale_bytes(rc, I, layout), dtype=torch.uint8, device=dev)
     yp = torch.empty(rc, d, dtype=torch.bfloat16, device=dev)
     gws = torch.zeros(256, dtype=torch.uint8, device=dev)
-    names = ["route_topk", "permute", "quant_mxfp8", "gemm_w13_glu", "gemm_w2", "combine"]
+    names = ["route_topk", "permute", "quant_mxfp4" if args.a4w4 else "quant_mxfp8",
+             "gemm_w13_glu", "gemm_w2", "combine"]
+    if args.a4w4:
+        quant_call = lambda: abi.moe_quant_mxfp4(x, T, d, s2r, k, xq, xs, rc, xs_layout)
+        w13_call = lambda: abi.moe_grouped_gemm_w13_glu_a4w4(
+            xq, xs, counts_d, offsets_d, E, d, I, layout, layer.w13, layer.w13_sf, hq, hs, rc, gws)
+    else:
+        quant_call = lambda: abi.moe_quant_mxfp8(x, T, d, s2r, k, xq, xs, rc, layout)
+        w13_call = lambda: abi.moe_grouped_gemm_w13_glu(xq, xs, counts_d, offsets_d, E, d, I,
+                                                        kernel, layer.w13, layer.w13_sf, hq, hs,
+                                                        rc, gws)
     calls = [
         lambda: abi.moe_route_topk(logits, T, E, k, ids, w),
         lambda: abi.moe_permute(ids, T, E, k, pad, counts_d, offsets_d, s2r, r2s, rc, pws),
-        lambda: abi.moe_quant_mxfp8(x, T, d, s2r, k, xq, xs, rc, layout),
-        lambda: abi.moe_grouped_gemm_w13_glu(xq, xs, counts_d, offsets_d, E, d, I, kernel,
-                                             layer.w13, layer.w13_sf, hq, hs, rc, gws),
+        quant_call,
+        w13_call,
         lambda: abi.moe_grouped_gemm_w2(hq, hs, counts_d, offsets_d, E, I, d, kernel, layer.w2,
                                         layer.w2_sf, yp, rc, gws),
         lambda: abi.moe_unpermute_combine(yp, s2r, w, T, k, d, y),
@@ -355,7 +370,7 @@ def main():
     for _ in range(3):
         x_d.copy_(x_h, non_blocking=True)
         lg_d.copy_(lg_h, non_blocking=True)
-        layer.forward(x_d, lg_d, ws=ws, y=y)
+        layer.forward(x_d, lg_d, ws=ws, y=y, a4w4=args.a4w4)
         y_h.copy_(y, non_blocking=True)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -365,7 +380,7 @@ def main():
             flush.fill_(i & 0xFF)
         x_d.copy_(x_h, non_blocking=True)
         lg_d.copy_(lg_h, non_blocking=True)
-        layer.forward(x_d, lg_d, ws=ws, y=y)
+        layer.forward(x_d, lg_d, ws=ws, y=y, a4w4=args.a4w4)
         y_h.copy_(y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -374,35 +389,39 @@ def main():
 
     peaks, peak_src = load_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * FP8_OVER_BF16
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tensor_peak = bf16_peak * FP8_OVER_BF16
+    w13_peak = bf16_peak * (FP4_OVER_BF16 if args.a4w4 else FP8_OVER_BF16)
     t_mem = U * expert_bytes / (hbm_peak * 1e9)
-    t_math = flops / (tensor_peak * 1e12)
+    t_math = 4.0 * T * k * d * I / (w13_peak * 1e12) + 2.0 * T * k * d * I / (tensor_peak * 1e12)
     bound = "hbm" if t_mem >= t_math else "tensor"
     ms_per_step = total_ms / args.steps
     layer_frac = max(t_mem, t_math) / (ms_per_step / 1e3)
     family = "weight_tiles" if kernel == abi.GEMM_WEIGHT_TILES else "token_tiles"
     dom = "gemm_w13_glu"
     dom_s = kms[dom] / 1e3
+    x_row_bytes = (d // 2 if args.a4w4 else d) + d // 32
     if bound == "hbm":
-        dom_bytes = U * w13_bytes + valid_rows * (d + d // 32) + valid_rows * (I + I // 32)
+        dom_bytes = U * w13_bytes + valid_rows * x_row_bytes + valid_rows * (I + I // 32)
         roof = {"kernel": dom, "bound": "hbm", "achieved": dom_bytes / dom_s / 1e9,
                 "peak": hbm_peak, "unit": "GB/s", "frac": dom_bytes / dom_s / 1e9 / hbm_peak,
-                "traffic": profiled_traffic(dom, wl.name, family),
+                "traffic": profiled_traffic(dom, wl.name, family) if not args.a4w4 else None,
                 "algorithmic_bytes": dom_bytes, "peak_source": peak_src}
     else:
         dom_flops = 4.0 * T * k * d * I
+        ratio, what = (FP4_OVER_BF16, "fp4") if args.a4w4 else (FP8_OVER_BF16, "fp8")
         roof = {"kernel": dom, "bound": "tensor", "achieved": dom_flops / dom_s / 1e12,
-                "peak": tensor_peak, "unit": "TFLOP/s",
-                "frac": dom_flops / dom_s / 1e12 / tensor_peak,
-                "traffic": profiled_traffic(dom, wl.name, family),
+                "peak": w13_peak, "unit": "TFLOP/s",
+                "frac": dom_flops / dom_s / 1e12 / w13_peak,
+                "traffic": profiled_traffic(dom, wl.name, family) if not args.a4w4 else None,
                 "algorithmic_flops": dom_flops,
-                "peak_source": peak_src + " bf16 x %.1f (fp8 / bf16 nominal ratio)" % FP8_OVER_BF16}
+                "peak_source": peak_src + " bf16 x %.1f (%s / bf16 nominal ratio)" % (ratio, what)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_sample or (T if T <= 64 else 32)
         cores = os.cpu_count() or 1
-        dt = oracle_seconds(wl, oracle_inputs(L, n), cores)
+        dt = oracle_seconds(wl, oracle_inputs(L, n), cores, a4w4=args.a4w4)
         cpu = {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": "first %d of %d tokens, full layer (%.1f s)" % (n, T, dt)}
 
@@ -414,12 +433,14 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "mxfp8(e4m3)xmxfp4(e2m1)->f32",
+            "dtype": ("stage1 mxfp4(e2m1)xmxfp4(e2m1)->f32, stage2 mxfp8(e4m3)xmxfp4(e2m1)->f32"
+                      if args.a4w4 else "mxfp8(e4m3)xmxfp4(e2m1)->f32"),
             "data": "synthetic (seeded; x~N(0,1) bf16, logits~N(0,1), uniform E2M1 codes, "
                     "E8M0 scales 118..122)",
             "config": {"workload": wl.name, "T": T, "d": d, "E": E, "k": k, "I": I,
                        "gemm_kernel": "weight_tiles" if kernel == abi.GEMM_WEIGHT_TILES
-                       else "token_tiles", "touched_experts": U, "padded_rows": padded_rows,
+                       else "token_tiles", "a4w4": bool(args.a4w4),
+                       "touched_experts": U, "padded_rows": padded_rows,
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": l2_note},
             "layer_roofline": {"bound": bound, "time_ms": 1e3 * max(t_mem, t_math),

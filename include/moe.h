@@ -284,7 +284,7 @@ moe_status moe_unpermute_combine(const uint16_t* yp, const int32_t* slot_to_row,
                                  const float* topk_w, int32_t T, int32_t k, int32_t d,
                                  uint16_t* y, cudaStream_t stream);
 
-/* Workspace bytes moe_forward needs for these dims. */
+/* Workspace bytes moe_forward and moe_forward_a4w4 need for these dims. */
 moe_status moe_workspace_size(const moe_dims* dims, size_t* bytes);
 
 /* The whole layer: route -> permute -> quantise -> stage-1 GEMM + GLU +
@@ -298,6 +298,45 @@ moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
                        const float* logits, const moe_weights* weights, uint16_t* y,
                        int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
                        cudaStream_t stream);
+
+/* ---- A4W4 stage 1 ---------------------------------------------------------
+ * The pages select their stage-1 MoE kernel with a switch named A4W4 next to
+ * the FP8 second-stage switch ("Appendix: environment variables" of "Kimi
+ * K3.1 Pro on AMD Instinct GPUs"): 4-bit activations with the 4-bit weights.
+ * These entry points run stage 1 with MXFP4 activations (E2M1 elements, one
+ * E8M0 scale per 32, shared exponent floor(log2(amax)) - 2, elements rounded
+ * to nearest even and saturated to +-6; -0 kept) on kind::mxf4 tensor cores;
+ * stage 2 is unchanged (MXFP8 h, the FP8 second stage). */
+
+/* MXFP4 quantisation of bf16 activations, otherwise as moe_quant_mxfp8:
+ * codes packed [rows_capacity][d/2] (even element in the low nibble of each
+ * byte, 4-byte aligned), scales in scale_layout for (rows_capacity, d). */
+moe_status moe_quant_mxfp4(const uint16_t* x, int32_t T, int32_t d, const int32_t* slot_to_row,
+                           int32_t k, uint8_t* codes, uint8_t* scales, int32_t scale_layout,
+                           int64_t rows_capacity, cudaStream_t stream);
+
+/* Stage 1 with MXFP4 activations (token tiles: groups padded to 128, xs
+ * TILED): g, u, h as in moe_grouped_gemm_w13_glu with X decoded from E2M1;
+ * h -> MXFP8 codes hq and scales hs in hs_layout (TILED for the token-tile
+ * stage 2, GROUP32 for the weight-tile stage 2). xq packed [rows_capacity][d/2];
+ * d % 256 == 0 (MOE_ERR_UNSUPPORTED otherwise). w13 and w13_sf, counts,
+ * offsets, alignment, padding rows and errors as moe_grouped_gemm_w13_glu. */
+moe_status moe_grouped_gemm_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs,
+                                         const int32_t* counts, const int32_t* offsets, int32_t E,
+                                         int32_t d, int32_t I, int32_t hs_layout,
+                                         const uint8_t* w13, const uint8_t* w13_sf, uint8_t* hq,
+                                         uint8_t* hs, int64_t rows_capacity, void* ws,
+                                         size_t ws_bytes, cudaStream_t stream);
+
+/* The whole layer with MXFP4 stage-1 activations: route -> permute (groups
+ * of 128) -> MXFP4 quantise -> A4W4 stage 1 + GLU + MXFP8 requant -> stage 2
+ * -> combine. kernel selects the stage-2 family (MOE_GEMM_AUTO =
+ * moe_default_kernel); stage 1 always runs on token tiles. d % 256 == 0.
+ * Other arguments as moe_forward. */
+moe_status moe_forward_a4w4(const moe_dims* dims, int32_t kernel, const uint16_t* x,
+                            const float* logits, const moe_weights* weights, uint16_t* y,
+                            int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                            cudaStream_t stream);
 
 /* Synchronises `stream`, then returns the status recorded in the workspace's
  * status word (MOE_OK if none). */

@@ -61,6 +61,11 @@ _SIGS = {
     "moe_workspace_size": (_i32, [ctypes.POINTER(_Dims), ctypes.POINTER(_sz)]),
     "moe_forward": (_i32, [ctypes.POINTER(_Dims), _i32, _vp, _vp, ctypes.POINTER(_Weights), _vp,
                            _vp, _vp, _vp, _sz, _vp]),
+    "moe_quant_mxfp4": (_i32, [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _i32, _i64, _vp]),
+    "moe_grouped_gemm_w13_glu_a4w4": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp,
+                                             _vp, _vp, _i64, _vp, _sz, _vp]),
+    "moe_forward_a4w4": (_i32, [ctypes.POINTER(_Dims), _i32, _vp, _vp, ctypes.POINTER(_Weights),
+                                _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_check_device_status": (_i32, [_vp, _vp]),
     "moe_clear_device_status": (_i32, [_vp, _vp]),
     "moe_selftest_wait_timeout": (_i32, [_vp, _sz, ctypes.c_uint32, _vp]),
@@ -205,6 +210,28 @@ def moe_forward(T, d, E, k, I, kernel, x, logits, w13, w13_sf, w2, w2_sf, y, ws,
                 topk_ids_out=None, topk_w_out=None, stream=None):
     W = _Weights(_ptr(w13), _ptr(w13_sf), _ptr(w2), _ptr(w2_sf))
     _call("moe_forward", ctypes.byref(_Dims(T, d, E, k, I)), kernel, _ptr(x), _ptr(logits),
+          ctypes.byref(W), _ptr(y), _ptr(topk_ids_out), _ptr(topk_w_out), _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def moe_quant_mxfp4(x, T, d, slot_to_row, k, codes, scales, rows_capacity, scale_layout=0,
+                    stream=None):
+    """MXFP4 activations: codes packed [rows_capacity][d/2]."""
+    _call("moe_quant_mxfp4", _ptr(x), T, d, _ptr(slot_to_row), k, _ptr(codes), _ptr(scales),
+          scale_layout, rows_capacity, _stream(stream))
+
+
+def moe_grouped_gemm_w13_glu_a4w4(xq, xs, counts, offsets, E, d, I, hs_layout, w13, w13_sf, hq,
+                                  hs, rows_capacity, ws, stream=None):
+    _call("moe_grouped_gemm_w13_glu_a4w4", _ptr(xq), _ptr(xs), _ptr(counts), _ptr(offsets), E, d,
+          I, hs_layout, _ptr(w13), _ptr(w13_sf), _ptr(hq), _ptr(hs), rows_capacity, _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def moe_forward_a4w4(T, d, E, k, I, kernel, x, logits, w13, w13_sf, w2, w2_sf, y, ws,
+                     topk_ids_out=None, topk_w_out=None, stream=None):
+    W = _Weights(_ptr(w13), _ptr(w13_sf), _ptr(w2), _ptr(w2_sf))
+    _call("moe_forward_a4w4", ctypes.byref(_Dims(T, d, E, k, I)), kernel, _ptr(x), _ptr(logits),
           ctypes.byref(W), _ptr(y), _ptr(topk_ids_out), _ptr(topk_w_out), _ptr(ws),
           ws.numel() * ws.element_size(), _stream(stream))
 

@@ -80,9 +80,10 @@ struct ForwardLayout {
   int64_t rows_cap;
 };
 
-ForwardLayout forward_layout(const moe_dims& D, int32_t kernel) {
-  const int32_t pad_m = group_pad(kernel);
-  const int32_t layout = scale_layout(kernel);
+// Workspace carve-up for one forward: groups padded to pad_m, activation
+// scales of x in xs_layout and of h in hs_layout.
+ForwardLayout forward_layout(const moe_dims& D, int32_t pad_m, int32_t xs_layout,
+                             int32_t hs_layout) {
   ForwardLayout L{};
   const size_t slots = size_t(D.T) * size_t(D.k);
   L.rows_cap = rows_capacity_of(D.T, D.E, D.k, pad_m);
@@ -102,12 +103,23 @@ ForwardLayout forward_layout(const moe_dims& D, int32_t kernel) {
   L.s2r = take(slots * 4);
   L.r2s = take(rc * 4);
   L.xq = take(rc * size_t(D.d));
-  L.xs = take(act_scale_bytes(L.rows_cap, D.d, layout));
+  L.xs = take(act_scale_bytes(L.rows_cap, D.d, xs_layout));
   L.hq = take(rc * size_t(D.I));
-  L.hs = take(act_scale_bytes(L.rows_cap, D.I, layout));
+  L.hs = take(act_scale_bytes(L.rows_cap, D.I, hs_layout));
   L.yp = take(rc * size_t(D.d) * 2);
   L.total = off;
   return L;
+}
+
+ForwardLayout forward_layout(const moe_dims& D, int32_t kernel) {
+  return forward_layout(D, group_pad(kernel), scale_layout(kernel), scale_layout(kernel));
+}
+
+// The A4W4 forward: stage 1 on token tiles (groups of 128, TILED x scales),
+// h scales in the layout of the stage-2 family.
+ForwardLayout forward_layout_a4w4(const moe_dims& D, int32_t stage2_kernel) {
+  return forward_layout(D, group_pad(MOE_GEMM_TOKEN_TILES), MOE_SCALES_TILED128,
+                        scale_layout(stage2_kernel));
 }
 
 moe_status check_dims(const moe_dims* D) {
@@ -265,6 +277,26 @@ moe_status moe_quant_mxfp8(const uint16_t* x, int32_t T, int32_t d, const int32_
       moe::launch_quant_mxfp8(x, T, d, slot_to_row, k, codes, scales, scale_layout, stream));
 }
 
+moe_status moe_quant_mxfp4(const uint16_t* x, int32_t T, int32_t d, const int32_t* slot_to_row,
+                           int32_t k, uint8_t* codes, uint8_t* scales, int32_t scale_layout,
+                           int64_t rows_capacity, cudaStream_t stream) {
+  if (T < 0 || k < 0 || rows_capacity < 0) return MOE_ERR_INVALID_ARGUMENT;
+  moe_status s = check_width(d);
+  if (s != MOE_OK) return s;
+  if (k > kMaxK || int64_t(T) * (k > 0 ? k : 1) >= int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  if (rows_capacity % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (scale_layout != MOE_SCALES_TILED128 && scale_layout != MOE_SCALES_GROUP32)
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0 || (slot_to_row && k == 0)) return MOE_OK;
+  if (!x || !codes || !scales) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || !aligned(codes, 4) || !aligned(scales, 4) ||
+      (slot_to_row && !aligned(slot_to_row, 4)))
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (!slot_to_row && rows_capacity < T) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(
+      moe::launch_quant_mxfp4(x, T, d, slot_to_row, k, codes, scales, scale_layout, stream));
+}
+
 moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int32_t* counts,
                                     const int32_t* offsets, int32_t E, int32_t d, int32_t I,
                                     int32_t kernel, const uint8_t* w13, const uint8_t* w13_sf,
@@ -280,6 +312,24 @@ moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const 
                                                      static_cast<int*>(ws), stream));
   return from_cuda(moe::launch_gemm_w13_glu(xq, xs, counts, offsets, E, d, I, w13, w13_sf, hq,
                                             hs, rows_capacity, static_cast<int*>(ws), stream));
+}
+
+moe_status moe_grouped_gemm_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs,
+                                         const int32_t* counts, const int32_t* offsets, int32_t E,
+                                         int32_t d, int32_t I, int32_t hs_layout,
+                                         const uint8_t* w13, const uint8_t* w13_sf, uint8_t* hq,
+                                         uint8_t* hs, int64_t rows_capacity, void* ws,
+                                         size_t ws_bytes, cudaStream_t stream) {
+  moe_status s = check_gemm_args(E, d, I, MOE_GEMM_TOKEN_TILES, rows_capacity, xq, xs, counts,
+                                 offsets, w13, w13_sf, hq, hs, true, ws, ws_bytes);
+  if (s != MOE_OK) return s;
+  if (d % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  if (hs_layout != MOE_SCALES_TILED128 && hs_layout != MOE_SCALES_GROUP32)
+    return MOE_ERR_UNSUPPORTED;
+  if (rows_capacity == 0) return MOE_OK;
+  return from_cuda(moe::launch_gemm_w13_glu_a4w4(xq, xs, counts, offsets, E, d, I, w13, w13_sf,
+                                                 hq, hs, hs_layout, rows_capacity,
+                                                 static_cast<int*>(ws), stream));
 }
 
 moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32_t* counts,
@@ -317,21 +367,33 @@ moe_status moe_workspace_size(const moe_dims* dims, size_t* bytes) {
   if (!bytes) return MOE_ERR_INVALID_ARGUMENT;
   moe_status s = check_dims(dims);
   if (s != MOE_OK) return s;
-  const size_t a = forward_layout(*dims, MOE_GEMM_TOKEN_TILES).total;
-  const size_t b = forward_layout(*dims, MOE_GEMM_WEIGHT_TILES).total;
-  *bytes = a > b ? a : b;
+  size_t m = 0;
+  for (const size_t t : {forward_layout(*dims, MOE_GEMM_TOKEN_TILES).total,
+                         forward_layout(*dims, MOE_GEMM_WEIGHT_TILES).total,
+                         forward_layout_a4w4(*dims, MOE_GEMM_TOKEN_TILES).total,
+                         forward_layout_a4w4(*dims, MOE_GEMM_WEIGHT_TILES).total})
+    m = t > m ? t : m;
+  *bytes = m;
   return MOE_OK;
 }
 
-moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
-                       const float* logits, const moe_weights* W, uint16_t* y,
-                       int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
-                       cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The layer, MXFP8 (a4w4 = false) or with MXFP4 stage-1 activations. kernel
+// is the GEMM family of both stages (MXFP8) or of stage 2 (A4W4, whose stage 1
+// always runs on token tiles).
+moe_status forward_impl(bool a4w4, const moe_dims* dims, int32_t kernel, const uint16_t* x,
+                        const float* logits, const moe_weights* W, uint16_t* y,
+                        int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
   moe_status s = check_dims(dims);
   if (s != MOE_OK) return s;
+  if (a4w4 && dims->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
   if (kernel == MOE_GEMM_AUTO) kernel = auto_kernel(dims->T, dims->E, dims->k);
   if (!kernel_ok(kernel)) return MOE_ERR_UNSUPPORTED;
-  const int32_t pad_m = group_pad(kernel);
+  const int32_t pad_m = group_pad(a4w4 ? int32_t(MOE_GEMM_TOKEN_TILES) : kernel);
   const moe_dims D = *dims;
   if (D.T == 0) return MOE_OK;
   if (!x || !logits || !W || !y || !ws || !W->w13 || !W->w13_sf || !W->w2 || !W->w2_sf)
@@ -341,7 +403,7 @@ moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
       !aligned(W->w2_sf, 16) || (topk_ids_out && !aligned(topk_ids_out, 4)) ||
       (topk_w_out && !aligned(topk_w_out, 4)))
     return MOE_ERR_INVALID_ARGUMENT;
-  const ForwardLayout L = forward_layout(D, kernel);
+  const ForwardLayout L = a4w4 ? forward_layout_a4w4(D, kernel) : forward_layout(D, kernel);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
 
   int* status = at<int>(ws, L.status);
@@ -366,6 +428,23 @@ moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
   if ((e = moe::launch_permute(ids, D.T, D.E, D.k, pad_m, counts, offsets, s2r, r2s, L.rows_cap,
                                at<int>(ws, L.hist), status, stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (a4w4) {
+    if ((e = moe::launch_quant_mxfp4(x, D.T, D.d, s2r, D.k, xq, xs, MOE_SCALES_TILED128,
+                                     stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if ((e = moe::launch_gemm_w13_glu_a4w4(xq, xs, counts, offsets, D.E, D.d, D.I, W->w13,
+                                           W->w13_sf, hq, hs, scale_layout(kernel), L.rows_cap,
+                                           status, stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (kernel == MOE_GEMM_WEIGHT_TILES)
+      e = moe::launch_gemm_decode_w2(hq, hs, counts, offsets, D.E, D.I, D.d, W->w2, W->w2_sf, yp,
+                                     L.rows_cap, status, stream);
+    else
+      e = moe::launch_gemm_w2(hq, hs, counts, offsets, D.E, D.I, D.d, W->w2, W->w2_sf, yp,
+                              L.rows_cap, status, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_combine(yp, s2r, w, D.T, D.k, D.d, y, stream));
+  }
   if ((e = moe::launch_quant_mxfp8(x, D.T, D.d, s2r, D.k, xq, xs, scale_layout(kernel),
                                    stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -386,6 +465,26 @@ moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
       return MOE_ERR_CUDA;
   }
   return from_cuda(moe::launch_combine(yp, s2r, w, D.T, D.k, D.d, y, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward(const moe_dims* dims, int32_t kernel, const uint16_t* x,
+                       const float* logits, const moe_weights* W, uint16_t* y,
+                       int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  return forward_impl(false, dims, kernel, x, logits, W, y, topk_ids_out, topk_w_out, ws,
+                      ws_bytes, stream);
+}
+
+moe_status moe_forward_a4w4(const moe_dims* dims, int32_t kernel, const uint16_t* x,
+                            const float* logits, const moe_weights* W, uint16_t* y,
+                            int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+  return forward_impl(true, dims, kernel, x, logits, W, y, topk_ids_out, topk_w_out, ws,
+                      ws_bytes, stream);
 }
 
 moe_status moe_check_device_status(const void* ws, cudaStream_t stream) {

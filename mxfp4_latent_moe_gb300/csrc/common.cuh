@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -34,14 +35,17 @@ constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 // MX rule (OCP MX v1.0) for MXFP8 = E4M3 elements + one E8M0 scale per 32.
 // ---------------------------------------------------------------------------
 
-// Scale code clamp(floor(log2(amax)) - 8 + 127, 0, 254); 0 for amax == 0.
-// floor(log2) is read exactly from the fp32 bit pattern (normal or subnormal).
+// Scale code clamp(floor(log2(amax)) - EMAX + 127, 0, 254); 0 for amax == 0.
+// EMAX is the exponent of the element format's largest power of two: 8 for
+// E4M3 (MXFP8), 2 for E2M1 (MXFP4). floor(log2) is read exactly from the fp32
+// bit pattern (normal or subnormal).
+template <int EMAX = 8>
 __device__ __forceinline__ int mx_scale_code(float amax) {
   const uint32_t b = __float_as_uint(amax);
   if (b == 0u) return 0;
   const int field = int(b >> 23) & 0xFF;
   const int fl = field ? field - 127 : (31 - __clz(int(b))) - 149;
-  const int code = fl - 8 + 127;
+  const int code = fl - EMAX + 127;
   return code < 0 ? 0 : (code > 254 ? 254 : code);
 }
 
@@ -59,6 +63,16 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   a = fabsf(a) < 0x1p-11f ? copysignf(0.0f, a) : a;
   b = fabsf(b) < 0x1p-11f ? copysignf(0.0f, b) : b;
   return uint32_t(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Two fp32 -> two E2M1 codes in one byte (a in the low nibble): round to
+// nearest even, saturate to +-6. Magnitudes below 0.25 round to zero anyway;
+// they are sent as a signed zero so the sign of zero results never depends on
+// the converter's handling of tiny or subnormal inputs.
+__device__ __forceinline__ uint32_t e2m1x2(float a, float b) {
+  a = fabsf(a) < 0.25f ? copysignf(0.0f, a) : a;
+  b = fabsf(b) < 0.25f ? copysignf(0.0f, b) : b;
+  return uint32_t(__nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest));
 }
 
 // Four scaled values -> four E4M3 codes packed little-endian.
@@ -289,6 +303,18 @@ __device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t saddr) {
   return d;
 }
 
+// Same for a K-major operand with 64-byte rows and 64-byte swizzle (8-row
+// atoms 512 bytes apart): the packed E2M1 weight boxes of the A4W4 GEMM.
+__device__ __forceinline__ uint64_t desc_sw64_kmajor(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= uint64_t(1) << 16;                  // leading byte offset (unused here)
+  d |= uint64_t(512 >> 4) << 32;           // stride byte offset: next 8-row atom
+  d |= uint64_t(1) << 46;                  // descriptor version (tcgen05)
+  d |= uint64_t(4) << 61;                  // 64-byte swizzle
+  return d;
+}
+
 // Descriptor of a scale-factor block: 32 rows x 16 bytes, no swizzle, 8-row
 // core matrices 128 bytes apart.
 __device__ __forceinline__ uint64_t desc_sf_block(uint32_t saddr) {
@@ -314,5 +340,24 @@ __host__ __device__ constexpr uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t
 
 constexpr uint32_t kFmtE4M3 = 0;
 constexpr uint32_t kFmtE2M1 = 5;
+// kind::mxf4 takes only E2M1 operands, coded 1 in its instruction descriptor
+// (same field positions as kind::mxf8f6f4; scale_vec::2X, UE8M0 scales: each
+// MMA of K = 64 reads two scale bytes per row starting at the byte its
+// scale-factor id selects, 0 or 2).
+constexpr uint32_t kFmtMxf4E2M1 = 1;
+
+// D(tmem) (+)= A(smem) x B(smem)^T, both packed E2M1 (K = 64 per MMA), two
+// E8M0 scale factors per row per MMA from tensor memory.
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
 
 }  // namespace moe

@@ -41,23 +41,29 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;            // rows per tile (MMA M)
-constexpr int BK = 128;            // inputs per pipeline stage
+constexpr int BK = 128;            // inputs per pipeline stage (MXFP8 activations)
+constexpr int BK4 = 256;           // inputs per pipeline stage (A4W4: MXFP4 activations)
 constexpr int BN = 256;            // MMA N
 constexpr int STAGES = 4;
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, 256)
-constexpr uint32_t kSfCol = 256;   // scale slots: 16 columns per stage (A: 4, B: 8)
-constexpr uint32_t A_BYTES = BM * BK;
-// E2M1 in shared memory: TMA's 16U4_ALIGN16B expansion puts each 16 codes
-// (8 packed bytes) in the low half of a 16-byte slot, so a 128-input row takes
+constexpr uint32_t kSfCol = 256;   // scale slots: 32 columns per stage
+// A: 128 rows x 128 bytes (128 E4M3 inputs, or 256 packed E2M1 inputs).
+constexpr uint32_t A_BYTES = BM * 128;
+// B, MXFP8 path: TMA's 16U4_ALIGN16B expansion puts each 16 E2M1 codes (8
+// packed bytes) in the low half of a 16-byte slot, so a 128-input row takes
 // 128 bytes of shared memory; the mbarrier transaction count is the packed
-// size, half of that.
-constexpr uint32_t B_BYTES = BN * BK;
+// size, half of that. A4W4 path: four packed 8 KB boxes (gate and up rows,
+// two 128-input halves), no expansion, the same 32 KB.
+constexpr uint32_t B_BYTES = BN * 128;
 constexpr uint32_t B_TX_BYTES = B_BYTES / 2;
-constexpr uint32_t SFA_BYTES = 512;
-constexpr uint32_t SFB_BYTES = 1024;
-constexpr uint32_t kStageTx = A_BYTES + B_TX_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr uint32_t B_BOX = 8192;   // one BOXED weight box: 128 rows x 64 bytes
+// scale atoms per stage: MXFP8 A 1, B 2; A4W4 A 2, B 4 (512 bytes each)
+constexpr uint32_t SFA_BYTES = 1024;
+constexpr uint32_t SFB_BYTES = 2048;
+constexpr uint32_t kStageTx = A_BYTES + B_TX_BYTES + 512 + 1024;
+constexpr uint32_t kStageTxA4 = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + STAGES * A_BYTES;
@@ -105,10 +111,13 @@ __device__ __forceinline__ void decode_tile(int tile, const int* prefix, const i
   row0 = offs[e] + (r - nt * mtiles) * BM;
 }
 
-template <int MODE>
+// MODE 0: w13 + GLU + MXFP8 requant of h (scales of h in layout HSL);
+// MODE 1: w2 -> bf16. A4: MXFP4 activations and kind::mxf4 (MODE 0 only).
+template <int MODE, bool A4, int HSL>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  static_assert(!A4 || MODE == 0, "the A4W4 path is stage 1 only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -126,7 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
-  const int KT = p.K / BK;
+  const int KT = p.K / (A4 ? BK4 : BK);   // pipeline stages per tile
+  const int KT128 = p.K / 128;            // 128-input tiles of the scale and weight layouts
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -203,30 +213,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sb = smem + kOffB + stage * B_BYTES;
           uint8_t* ssfa = smem + kOffSfa + stage * SFA_BYTES;
           uint8_t* ssfb = smem + kOffSfb + stage * SFB_BYTES;
-          const uint8_t* gsfa = p.a_sf + (int64_t(row0 >> 7) * KT + kt) * 512;
-          if (MODE == 0) {
+          const uint8_t* gsfa = p.a_sf + (int64_t(row0 >> 7) * KT128 + kt) * 512;
+          if (A4) {
+            // packed activations: one 128-byte box row = 256 inputs; weights:
+            // the gate and up boxes of both 128-input halves, 64-byte swizzle
+            const int64_t g_rt = (int64_t(e) * 2 * p.I + int64_t(nt) * 128) >> 7;
+            const int64_t u_rt = g_rt + (p.I >> 7);
+            mbar_arrive_expect_tx(&full[stage], kStageTxA4);
+            tma_load_2d(sa, &tmap_a, &full[stage], kt * 128, row0);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              tma_load_2d(sb + h * 2 * B_BOX, &tmap_b, &full[stage], 0,
+                          boxed_row(g_rt, 2 * kt + h, KT128));
+              tma_load_2d(sb + h * 2 * B_BOX + B_BOX, &tmap_b, &full[stage], 0,
+                          boxed_row(u_rt, 2 * kt + h, KT128));
+            }
+            bulk_load(ssfa, p.a_sf + (int64_t(row0 >> 7) * KT128 + 2 * kt) * 512, 1024,
+                      &full[stage]);
+            bulk_load(ssfb, p.b_sf + (g_rt * KT128 + 2 * kt) * 512, 1024, &full[stage]);
+            bulk_load(ssfb + 1024, p.b_sf + (u_rt * KT128 + 2 * kt) * 512, 1024, &full[stage]);
+          } else if (MODE == 0) {
             const int64_t g_row = int64_t(e) * 2 * p.I + int64_t(nt) * 128;
             const int64_t u_row = g_row + p.I;
             mbar_arrive_expect_tx(&full[stage], kStageTx);
             tma_load_2d(sa, &tmap_a, &full[stage], kt * BK, row0);
-            tma_load_2d(sb, &tmap_b, &full[stage], 0, boxed_row(g_row >> 7, kt, KT));
-            tma_load_2d(sb + B_BYTES / 2, &tmap_b, &full[stage], 0, boxed_row(u_row >> 7, kt, KT));
-            bulk_load(ssfa, gsfa, SFA_BYTES, &full[stage]);
-            bulk_load(ssfb, p.b_sf + ((g_row >> 7) * KT + kt) * 512, 512, &full[stage]);
-            bulk_load(ssfb + 512, p.b_sf + ((u_row >> 7) * KT + kt) * 512, 512, &full[stage]);
+            tma_load_2d(sb, &tmap_b, &full[stage], 0, boxed_row(g_row >> 7, kt, KT128));
+            tma_load_2d(sb + B_BYTES / 2, &tmap_b, &full[stage], 0,
+                        boxed_row(u_row >> 7, kt, KT128));
+            bulk_load(ssfa, gsfa, 512, &full[stage]);
+            bulk_load(ssfb, p.b_sf + ((g_row >> 7) * KT128 + kt) * 512, 512, &full[stage]);
+            bulk_load(ssfb + 512, p.b_sf + ((u_row >> 7) * KT128 + kt) * 512, 512, &full[stage]);
           } else {
             const int64_t b_row = int64_t(e) * p.d + int64_t(nt) * BN;
             const bool upper = nt * BN + 128 < p.d;
             mbar_arrive_expect_tx(&full[stage], kStageTx - (upper ? 0u : 512u + B_TX_BYTES / 2));
             tma_load_2d(sa, &tmap_a, &full[stage], kt * BK, row0);
-            tma_load_2d(sb, &tmap_b, &full[stage], 0, boxed_row(b_row >> 7, kt, KT));
+            tma_load_2d(sb, &tmap_b, &full[stage], 0, boxed_row(b_row >> 7, kt, KT128));
             if (upper)
               tma_load_2d(sb + B_BYTES / 2, &tmap_b, &full[stage], 0,
-                          boxed_row((b_row >> 7) + 1, kt, KT));
-            bulk_load(ssfa, gsfa, SFA_BYTES, &full[stage]);
-            bulk_load(ssfb, p.b_sf + ((b_row >> 7) * KT + kt) * 512, 512, &full[stage]);
+                          boxed_row((b_row >> 7) + 1, kt, KT128));
+            bulk_load(ssfa, gsfa, 512, &full[stage]);
+            bulk_load(ssfb, p.b_sf + ((b_row >> 7) * KT128 + kt) * 512, 512, &full[stage]);
             if (upper)
-              bulk_load(ssfb + 512, p.b_sf + (((b_row >> 7) + 1) * KT + kt) * 512, 512,
+              bulk_load(ssfb + 512, p.b_sf + (((b_row >> 7) + 1) * KT128 + kt) * 512, 512,
                         &full[stage]);
           }
         }
@@ -253,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Converged warp; the elected lane issues every tcgen05 instruction (a
     // commit tracks the operations of the thread that issues it).
     const bool leader = elect_one_sync();
-    const uint32_t idesc = idesc_mxf8f6f4(kFmtE4M3, kFmtE2M1, BM, BN);
+    const uint32_t idesc = A4 ? idesc_mxf8f6f4(kFmtMxf4E2M1, kFmtMxf4E2M1, BM, BN)
+                              : idesc_mxf8f6f4(kFmtE4M3, kFmtE2M1, BM, BN);
     uint32_t stage = 0, phase = 0, acc_phase = 0;
     bool failed = false;
     for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
@@ -268,12 +298,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        if (leader) {
+        if (leader && A4) {
           const uint32_t sa = smem_u32(smem + kOffA + stage * A_BYTES);
           const uint32_t sb = smem_u32(smem + kOffB + stage * B_BYTES);
           const uint32_t ssfa = smem_u32(smem + kOffSfa + stage * SFA_BYTES);
           const uint32_t ssfb = smem_u32(smem + kOffSfb + stage * SFB_BYTES);
-          const uint32_t sfa_t = tmem_base + kSfCol + stage * 16;
+          // tensor-memory scale slots: A half h at +4h; B half h at +8+8h
+          // (gate rows), +12+8h (up rows = MMA rows 128..255)
+          const uint32_t sfa_t = tmem_base + kSfCol + stage * 32;
+          const uint32_t sfb_t = sfa_t + 8;
+          tc_cp_32x128b_x4(sfa_t, desc_sf_block(ssfa));
+          tc_cp_32x128b_x4(sfa_t + 4, desc_sf_block(ssfa + 512));
+          tc_cp_32x128b_x4(sfb_t, desc_sf_block(ssfb));
+          tc_cp_32x128b_x4(sfb_t + 4, desc_sf_block(ssfb + 1024));
+          tc_cp_32x128b_x4(sfb_t + 8, desc_sf_block(ssfb + 512));
+          tc_cp_32x128b_x4(sfb_t + 12, desc_sf_block(ssfb + 1536));
+          const uint64_t adesc = desc_sw128_kmajor(sa);
+#pragma unroll
+          for (int j = 0; j < BK4 / 64; ++j) {
+            // MMA j: inputs [64j, 64j+64) of the stage = 32 bytes of each row;
+            // A: +32j bytes in its 128-byte swizzle row; B: half j/2, +32(j%2)
+            // bytes in the 64-byte rows; scale bytes 2(j%2), 2(j%2)+1 of half j/2
+            const int h = j >> 1;
+            const uint64_t bdesc = desc_sw64_kmajor(sb + uint32_t(h) * 2 * B_BOX);
+            tc_mma_mxf4(tmem_base + kAccCol, adesc + uint64_t(2 * j),
+                        bdesc + uint64_t(2 * (j & 1)),
+                        idesc_with_sf_id(idesc, uint32_t(2 * (j & 1))), sfa_t + 4 * h,
+                        sfb_t + 8 * h, (kt > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+        } else if (leader) {
+          const uint32_t sa = smem_u32(smem + kOffA + stage * A_BYTES);
+          const uint32_t sb = smem_u32(smem + kOffB + stage * B_BYTES);
+          const uint32_t ssfa = smem_u32(smem + kOffSfa + stage * SFA_BYTES);
+          const uint32_t ssfb = smem_u32(smem + kOffSfb + stage * SFB_BYTES);
+          const uint32_t sfa_t = tmem_base + kSfCol + stage * 32;
           const uint32_t sfb_t = sfa_t + 4;
           tc_cp_32x128b_x4(sfa_t, desc_sf_block(ssfa));
           tc_cp_32x128b_x4(sfb_t, desc_sf_block(ssfb));
@@ -381,9 +440,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           sword |= uint32_t(code) << (8 * c);
         }
-        if (live)
-          *reinterpret_cast<uint16_t*>(
-              p.out_sf + tiled_sf_offset(row, int64_t(nt) * 4 + 2 * half, p.I)) = uint16_t(sword);
+        if (live) {
+          const int64_t b = int64_t(nt) * 4 + 2 * half;   // first of the two 32-blocks
+          const int64_t off = HSL == kScalesGroup32 ? group32_sf_offset(row, b, p.I)
+                                                    : tiled_sf_offset(row, b, p.I);
+          *reinterpret_cast<uint16_t*>(p.out_sf + off) = uint16_t(sword);
+        }
       } else if (active && live) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -424,10 +486,10 @@ __global__ void wait_timeout_selftest_kernel(int* status, uint64_t limit_ns) {
   }
 }
 
-template <int MODE>
+template <int MODE, bool A4 = false, int HSL = kScalesTiled128>
 cudaError_t launch_mode(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                         cudaStream_t st) {
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, A4, HSL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
   if (err != cudaSuccess) return err;
@@ -435,7 +497,7 @@ cudaError_t launch_mode(const GemmParams& p, const CUtensorMap& ta, const CUtens
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = int(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
-  grouped_gemm_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(ta, tb, p);
+  grouped_gemm_kernel<MODE, A4, HSL><<<grid, kThreads, kSmemBytes, st>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
@@ -493,6 +555,22 @@ bool encode_boxed_weights(CUtensorMap* map, const void* base, int64_t rows, int 
   return r == CUDA_SUCCESS;
 }
 
+// The same BOXED weights as packed bytes for the A4W4 GEMM: 64-byte rows
+// (128 E2M1 inputs) read as UINT8 with 64-byte swizzle, no expansion.
+bool encode_boxed_weights_packed(CUtensorMap* map, const void* base, int64_t rows, int K) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {64u, cuuint64_t(rows / 128) * cuuint64_t(K / 128) * 128u};
+  const cuuint64_t strides[1] = {64u};
+  const cuuint32_t box[2] = {64u, 128u};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -522,6 +600,33 @@ cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int*
   p.out_sf = hs;
   p.status = status;
   return launch_mode<0>(p, ta, tb, st);
+}
+
+cudaError_t launch_gemm_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs, const int* counts,
+                                     const int* offsets, int E, int d, int I, const uint8_t* w13,
+                                     const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
+                                     int hs_layout, int64_t rows_capacity, int* status,
+                                     cudaStream_t st) {
+  CUtensorMap ta, tb;
+  // packed activations: d/2 bytes per row, 128-byte boxes of 128 rows
+  if (!encode_operand(&ta, xq, false, d / 2, rows_capacity, BM)) return cudaErrorInvalidValue;
+  if (!encode_boxed_weights_packed(&tb, w13, int64_t(E) * 2 * I, d)) return cudaErrorInvalidValue;
+  GemmParams p{};
+  p.a_sf = xs;
+  p.b_sf = w13_sf;
+  p.counts = counts;
+  p.offsets = offsets;
+  p.E = E;
+  p.K = d;
+  p.I = I;
+  p.d = d;
+  p.n_tiles = I / 128;
+  p.rows_capacity = rows_capacity;
+  p.out_q = hq;
+  p.out_sf = hs;
+  p.status = status;
+  if (hs_layout == kScalesGroup32) return launch_mode<0, true, kScalesGroup32>(p, ta, tb, st);
+  return launch_mode<0, true, kScalesTiled128>(p, ta, tb, st);
 }
 
 cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* counts,

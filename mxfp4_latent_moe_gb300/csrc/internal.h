@@ -16,6 +16,8 @@ cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* 
 
 cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
                                uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st);
+cudaError_t launch_quant_mxfp4(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
+                               uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st);
 cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
                                   cudaStream_t st);
 cudaError_t launch_prepack_weights(const uint8_t* src, int64_t rows, int K, uint8_t* dst,
@@ -25,6 +27,13 @@ cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int*
                                 const int* offsets, int E, int d, int I, const uint8_t* w13,
                                 const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
                                 int64_t rows_capacity, int* status, cudaStream_t st);
+// A4W4 stage 1 (token tiles only): MXFP4 activations xq [rows][d/2] with
+// TILED scales, hs written in hs_layout (TILED or GROUP32).
+cudaError_t launch_gemm_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs, const int* counts,
+                                     const int* offsets, int E, int d, int I, const uint8_t* w13,
+                                     const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
+                                     int hs_layout, int64_t rows_capacity, int* status,
+                                     cudaStream_t st);
 cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* counts,
                            const int* offsets, int E, int I, int d, const uint8_t* w2,
                            const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity, int* status,

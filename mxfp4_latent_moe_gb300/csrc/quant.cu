@@ -1,5 +1,5 @@
-// MXFP8 quantisation of the stage-1 activations and the one-time scale
-// prepack of the MXFP4 weights.
+// MXFP8 (and, for the A4W4 stage 1, MXFP4) quantisation of the stage-1
+// activations and the one-time prepack of the MXFP4 weights.
 //
 // MX rule (OCP MX v1.0; the pages' layer keeps its routed experts in MXFP4
 // with one E8M0 scale per 32 values and runs an FP8 second stage, "Kimi K3.1
@@ -74,6 +74,53 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
+// MXFP4 (the A4W4 stage-1 activations): the same work layout with E2M1
+// elements and shared exponent floor(log2(amax)) - 2; a thread's 8 codes are
+// one 32-bit word of the packed [rows][d/2] output (even element in the low
+// nibble of each byte).
+template <int LAYOUT>
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_mxfp4_kernel(const uint4* __restrict__ x, int d, const int* __restrict__ slot_to_row,
+                       int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                       int64_t total_vec) {
+  const int64_t g = int64_t(blockIdx.x) * kQuantThreads + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const bool valid = g < total_vec;
+  const int vpr = d >> 3;
+  uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+  if (valid) raw = __ldg(x + g);
+  float f[8];
+  bf16x8_to_f32(raw, f);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const int code = mx_scale_code<2>(amax);
+  const float m = mx_scale_mult(code);
+  const uint32_t packed = e2m1x2(f[0] * m, f[1] * m) | (e2m1x2(f[2] * m, f[3] * m) << 8) |
+                          (e2m1x2(f[4] * m, f[5] * m) << 16) | (e2m1x2(f[6] * m, f[7] * m) << 24);
+  const int base = lane & ~15;
+  const uint32_t s0 = __shfl_sync(0xffffffffu, code, base);
+  const uint32_t s1 = __shfl_sync(0xffffffffu, code, base + 4);
+  const uint32_t s2 = __shfl_sync(0xffffffffu, code, base + 8);
+  const uint32_t s3 = __shfl_sync(0xffffffffu, code, base + 12);
+  if (!valid) return;
+  const uint32_t sword = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  const int64_t t = g / vpr;
+  const int v = int(g - t * vpr);
+  const int nrows = slot_to_row ? k : 1;
+  for (int j = 0; j < nrows; ++j) {
+    const int64_t row = slot_to_row ? int64_t(__ldg(slot_to_row + t * k + j)) : t;
+    *reinterpret_cast<uint32_t*>(codes + row * (d >> 1) + int64_t(v) * 4) = packed;
+    if ((lane & 15) == 0) {
+      const int64_t off = LAYOUT == kScalesGroup32 ? group32_sf_offset(row, int64_t(v >> 2), d)
+                                                   : tiled_sf_offset(row, int64_t(v >> 2), d);
+      *reinterpret_cast<uint32_t*>(scales + off) = sword;
+    }
+  }
+}
+
 // canonical [rows][K/32] -> TILED; one thread per 32-bit output word.
 __global__ void prepack_scales_kernel(const uint8_t* __restrict__ src, int64_t rows, int K,
                                       uint8_t* __restrict__ dst, int64_t words) {
@@ -118,6 +165,20 @@ cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_
         reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
   else
     quant_mxfp8_kernel<kScalesTiled128><<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mxfp4(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
+                               uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st) {
+  const int64_t total = int64_t(T) * (d / 8);
+  if (total == 0 || (slot_to_row && k == 0)) return cudaSuccess;
+  const int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
+  if (layout == kScalesGroup32)
+    quant_mxfp4_kernel<kScalesGroup32><<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
+  else
+    quant_mxfp4_kernel<kScalesTiled128><<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
         reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
   return cudaGetLastError();
 }

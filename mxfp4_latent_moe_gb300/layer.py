@@ -45,12 +45,16 @@ class MoeLayer:
         n = abi.moe_workspace_size(T, self.d, self.E, self.k, self.I)
         return torch.empty(n, dtype=torch.uint8, device=self.w13.device)
 
-    def forward(self, x, logits, ws=None, y=None, topk_ids=None, topk_w=None, stream=None):
+    def forward(self, x, logits, ws=None, y=None, topk_ids=None, topk_w=None, stream=None,
+                a4w4=False):
+        """y = the layer on x. a4w4: MXFP4 stage-1 activations (moe_forward_a4w4;
+        the kernel family then applies to stage 2)."""
         T = x.shape[0]
         if ws is None:
             ws = self.workspace(T)
         if y is None:
             y = torch.empty(T, self.d, dtype=torch.bfloat16, device=x.device)
-        abi.moe_forward(T, self.d, self.E, self.k, self.I, self.kernel_for(T), x, logits, self.w13,
-                        self.w13_sf, self.w2, self.w2_sf, y, ws, topk_ids, topk_w, stream)
+        fn = abi.moe_forward_a4w4 if a4w4 else abi.moe_forward
+        fn(T, self.d, self.E, self.k, self.I, self.kernel_for(T), x, logits, self.w13, self.w13_sf,
+           self.w2, self.w2_sf, y, ws, topk_ids, topk_w, stream)
         return y

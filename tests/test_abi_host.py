@@ -121,6 +121,22 @@ def test_host_validation_rejects_before_any_launch(L):
                None, fake, 10 ** 9, None) == abi.UNSUPPORTED
     assert _rc(L, "moe_forward", ctypes.byref(dims), 0, fake, fake, ctypes.byref(W), fake, None,
                None, fake, 10, None) == abi.WORKSPACE_TOO_SMALL
+    # A4W4: quant layout, d not a multiple of 256, bad hs layout, misaligned codes
+    assert _rc(L, "moe_quant_mxfp4", fake, 4, 256, None, 0, fake, fake, 3, 128, None) == \
+        abi.UNSUPPORTED
+    assert _rc(L, "moe_quant_mxfp4", fake, 4, 256, None, 0, ctypes.c_void_p(4098), fake, 0, 128,
+               None) == abi.INVALID_ARGUMENT
+    assert _rc(L, "moe_grouped_gemm_w13_glu_a4w4", fake, fake, fake, fake, E, 384, 3072, 0, fake,
+               fake, fake, fake, 1024, fake, 256, None) == abi.UNSUPPORTED      # d % 256
+    assert _rc(L, "moe_grouped_gemm_w13_glu_a4w4", fake, fake, fake, fake, E, 3584, 3072, 2, fake,
+               fake, fake, fake, 1024, fake, 256, None) == abi.UNSUPPORTED      # hs layout
+    assert _rc(L, "moe_grouped_gemm_w13_glu_a4w4", fake, fake, fake, fake, E, 3584, 3072, 0, fake,
+               fake, fake, fake, 1024, fake, 8, None) == abi.WORKSPACE_TOO_SMALL
+    dims_a4 = abi._Dims(4, 384, 896, 16, 3072)
+    assert _rc(L, "moe_forward_a4w4", ctypes.byref(dims_a4), 0, fake, fake, ctypes.byref(W), fake,
+               None, None, fake, 10 ** 9, None) == abi.UNSUPPORTED               # d % 256
+    assert _rc(L, "moe_forward_a4w4", ctypes.byref(dims), 0, fake, fake, ctypes.byref(W), fake,
+               None, None, fake, 10, None) == abi.WORKSPACE_TOO_SMALL
     # status helpers
     assert _rc(L, "moe_check_device_status", None, None) == abi.INVALID_ARGUMENT
     assert _rc(L, "moe_selftest_wait_timeout", fake, 8, 100, None) == abi.WORKSPACE_TOO_SMALL
