@@ -34,6 +34,10 @@ METRIC = "MoE-layer tokens/s and % roofline (HBM GB/s decode, tensor TFLOP/s pre
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense ratio: kind::mxf8f6f4 runs at the FP8 rate
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio: kind::mxf4 (A4W4 stage 1) runs at the FP4 rate
+# Measured on GB300 with a tensor-rate probe: an M=128, N=256 MMA issues every
+# 128 cycles in both kind::mxf8f6f4 (K=32) and kind::mxf4 (K=64), i.e. the
+# MXFP4 x MXFP4 rate is 2x the MXFP8 x MXFP4 rate, bf16 x 4 (not the nominal 6).
+FP4_MMA_OVER_BF16 = 2 * FP8_OVER_BF16
 
 
 def parse():
@@ -416,6 +420,10 @@ def main():
                 "traffic": profiled_traffic(dom, wl.name, family) if not args.a4w4 else None,
                 "algorithmic_flops": dom_flops,
                 "peak_source": peak_src + " bf16 x %.1f (%s / bf16 nominal ratio)" % (ratio, what)}
+        if args.a4w4:
+            mma_peak = bf16_peak * FP4_MMA_OVER_BF16
+            roof["frac_of_measured_mma_rate"] = dom_flops / dom_s / 1e12 / mma_peak
+            roof["measured_mma_rate_peak"] = mma_peak
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
