@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 8 * 32);
+    mbar_init(acc_empty, 8);   // one arrival per epilogue warp
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -407,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(acc_empty);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);   // the whole warp has read its part
       acc_phase ^= 1u;
       if (MODE == 0) {
         uint32_t sword = 0;

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 8 * 32);
+      mbar_init(&acc_empty[b], 8);   // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -326,7 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (two) tmem_ld_32x32b_x16(tq + kAcc1Col, v1);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&acc_empty[buf]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);   // the whole warp has read its part
       acc_phases ^= 1u << buf;
       buf ^= 1;
       // rows of the chunk past the expert's tokens are padding: not stored
