@@ -391,6 +391,26 @@ def main():
     sampler.stop()
     e2e_ms = replicas.max_over_ranks(e0.elapsed_time(e1), dev)
 
+    # ---- the same end to end with the step captured as one CUDA graph
+    graph, y_g, _ = layer.capture(x_d, lg_d, ws=ws, a4w4=args.a4w4)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        graph.replay()
+        y_h.copy_(y_g, non_blocking=True)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    e2e_graph_ms = replicas.max_over_ranks(g0.elapsed_time(g1), dev)
+    if abi.moe_check_device_status(ws) != abi.OK:
+        raise RuntimeError("device status error in the graph replays")
+
     peaks, peak_src = load_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -461,6 +481,9 @@ def main():
                     "unit": "tokens/s",
                     "h2d_bytes_per_step": T * d * 2 + T * E * 4,
                     "d2h_bytes_per_step": T * d * 2},
+            "e2e_graph": {"value": replicas.aggregate_rate(T, world, args.steps, e2e_graph_ms),
+                          "unit": "tokens/s", "how": "same copies, the step replayed as one "
+                          "CUDA graph (MoeLayer.capture)"},
             "cpu_baseline": cpu,
             "clocks": sampler.summary(),
         }

@@ -58,3 +58,24 @@ class MoeLayer:
         fn(T, self.d, self.E, self.k, self.I, self.kernel_for(T), x, logits, self.w13, self.w13_sf,
            self.w2, self.w2_sf, y, ws, topk_ids, topk_w, stream)
         return y
+
+    def capture(self, x, logits, ws=None, y=None, topk_ids=None, topk_w=None, a4w4=False):
+        """Records one forward on the given (static) buffers as a CUDA graph.
+
+        The layer's entry points are stream-ordered and neither allocate nor
+        synchronise, so the whole step (status reset, routing, grouping,
+        quantisation, both GEMMs, combine) becomes one graph launch. Refill x
+        and logits in place and call the returned graph's replay(); y (and the
+        routing outputs, if given) hold the result. One eager call runs first
+        so one-time host set-up happens outside the capture."""
+        T = x.shape[0]
+        if ws is None:
+            ws = self.workspace(T)
+        if y is None:
+            y = torch.empty(T, self.d, dtype=torch.bfloat16, device=x.device)
+        self.forward(x, logits, ws=ws, y=y, topk_ids=topk_ids, topk_w=topk_w, a4w4=a4w4)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.forward(x, logits, ws=ws, y=y, topk_ids=topk_ids, topk_w=topk_w, a4w4=a4w4)
+        return g, y, ws
