@@ -48,6 +48,8 @@ def lib():
                                        _u8p, _u8p, _u8p, _u8p, _u16p, _i32p, _f32p, _f64p, _i32]),
             "orc_expert_bytes": (_i64, [_i32, _i32]),
             "orc_e2m1_encode_rne_sat": (ctypes.c_uint8, [ctypes.c_double]),
+            "orc_gemm_bf16": (None, [_u16p, _u16p, _i64, _i64, _i64, _f64p]),
+            "orc_gemm_bf16_swiglu": (None, [_u16p, _u16p, _i64, _i64, _i64, _f64p]),
             "orc_mxfp4_quant_block": (None, [_f32p, _u8p, _u8p]),
             "orc_mxfp4_quant_rows": (None, [_f32p, _i64, _i64, _u8p, _u8p]),
             "orc_mxfp4_quant_rows_bf16": (None, [_u16p, _i64, _i64, _u8p, _u8p]),
@@ -221,6 +223,26 @@ def moe_forward(x_bits, logits, k, w13, w13s, w2, w2s, threads=0, want_y64=False
        _p(w2, _u8p), _p(w2s, _u8p), _p(y, _u16p), _p(ids, _i32p), _p(w, _f32p), _p(y64, _f64p),
        threads)
     return dict(y=y, ids=ids[:, :k], w=w[:, :k], y64=y64)
+
+
+def gemm_bf16(a_bits, b_bits):
+    """C = A . B^T in fp64; a_bits [M][K], b_bits [N][K] bf16 bit patterns."""
+    a, b = _c(a_bits, np.uint16), _c(b_bits, np.uint16)
+    M, K = a.shape
+    N = b.shape[0]
+    c = np.empty((M, N), np.float64)
+    lib().orc_gemm_bf16(_p(a, _u16p), _p(b, _u16p), M, N, K, _p(c, _f64p))
+    return c
+
+
+def gemm_bf16_swiglu(a_bits, b_bits):
+    """h = silu(A . Bgate^T) * (A . Bup^T) in fp64; b_bits [2*Nh][K], gate rows first."""
+    a, b = _c(a_bits, np.uint16), _c(b_bits, np.uint16)
+    M, K = a.shape
+    Nh = b.shape[0] // 2
+    h = np.empty((M, Nh), np.float64)
+    lib().orc_gemm_bf16_swiglu(_p(a, _u16p), _p(b, _u16p), M, Nh, K, _p(h, _f64p))
+    return h
 
 
 def expert_bytes(d, I):

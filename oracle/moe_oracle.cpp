@@ -408,6 +408,33 @@ void orc_moe_forward_a4w4(const uint16_t* x, const float* logits, int64_t n, int
                    threads);
 }
 
+// A dense product of bf16 operands, one fp64 dot product per output.
+void orc_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int64_t N, int64_t K,
+                   double* c) {
+  std::vector<double> ar(static_cast<size_t>(K));
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t t = 0; t < K; ++t) ar[size_t(t)] = double(bf16_bits_to_float(a[m * K + t]));
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t t = 0; t < K; ++t) acc += ar[size_t(t)] * double(bf16_bits_to_float(b[n * K + t]));
+      c[m * N + n] = acc;
+    }
+  }
+}
+
+// The gated MLP step: gate rows [0, Nh) and up rows [Nh, 2 Nh) of B.
+void orc_gemm_bf16_swiglu(const uint16_t* a, const uint16_t* b, int64_t M, int64_t Nh,
+                          int64_t K, double* h) {
+  std::vector<double> gu(static_cast<size_t>(2 * Nh));
+  for (int64_t m = 0; m < M; ++m) {
+    orc_gemm_bf16(a + m * K, b, 1, 2 * Nh, K, gu.data());
+    for (int64_t n = 0; n < Nh; ++n) {
+      const double g = gu[size_t(n)], u = gu[size_t(Nh + n)];
+      h[m * Nh + n] = g * sigmoid(g) * u;
+    }
+  }
+}
+
 int64_t orc_expert_bytes(int32_t d, int32_t I) {
   // Three I x d matrices: d*I/2 bytes of packed E2M1 and d*I/32 scale bytes each.
   return int64_t(3) * (int64_t(d) * I / 2 + int64_t(d) * I / 32);

@@ -137,6 +137,24 @@ void orc_moe_forward_a4w4(const uint16_t* x, const float* logits, int64_t n,
                           uint16_t* y, int32_t* ids, float* w, double* y64,
                           int32_t threads);
 
+/* ---- Neighbouring BF16 steps ------------------------------------------------
+ * The pages run the router GEMM producing the logits, the latent down/up
+ * projections (7,168 <-> 3,584) and two shared experts in BF16 next to the
+ * routed experts ("Kimi K3.1 Pro at a glance" and "The MXFP4 latent MoE on
+ * FlyDSL" of "Kimi K3.1 Pro on AMD Instinct GPUs"; "HBM Usage Under TP8" of
+ * "Day 0 Kimi-K3 Inference Deployment with ATOM on AMD Instinct MI355X
+ * GPUs"). Each is a dense product of bf16 operands. */
+
+/* C[M][N] = A[M][K] . B[N][K]^T in fp64 from bf16 bit patterns. */
+void orc_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int64_t N, int64_t K,
+                   double* c);
+
+/* The gated MLP step of a shared expert: B holds 2*Nh rows, gate rows first
+ * then up rows; h[M][Nh] = silu(g) * u with g = A . Bgate^T, u = A . Bup^T,
+ * all in fp64. */
+void orc_gemm_bf16_swiglu(const uint16_t* a, const uint16_t* b, int64_t M, int64_t Nh,
+                          int64_t K, double* h);
+
 /* Round a real number to the nearest bf16 (ties to even), returning its bits. */
 uint16_t orc_bf16_rne(double v);
 
