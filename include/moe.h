@@ -338,6 +338,37 @@ moe_status moe_forward_a4w4(const moe_dims* dims, int32_t kernel, const uint16_t
                             int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
                             cudaStream_t stream);
 
+/* ---- Neighbouring BF16 steps ------------------------------------------------
+ * The pages' layer runs its router GEMM, the latent down/up projections
+ * (7,168 <-> 3,584) and two shared experts in BF16 beside the MXFP4 routed
+ * experts ("Kimi K3.1 Pro at a glance" and "The MXFP4 latent MoE on FlyDSL"
+ * of "Kimi K3.1 Pro on AMD Instinct GPUs"; "HBM Usage Under TP8" of "Day 0
+ * Kimi-K3 Inference Deployment with ATOM on AMD Instinct MI355X GPUs"). They
+ * are dense products C = A . B^T of bf16 operands with fp32 accumulation on
+ * tcgen05 tensor cores (kind::f16). */
+typedef enum {
+  MOE_EPI_F32 = 0,          /* C fp32 [M][N] (router logits) */
+  MOE_EPI_BF16 = 1,         /* C bf16 [M][N], round to nearest even */
+  MOE_EPI_SWIGLU_BF16 = 2   /* B = N/2 gate rows then N/2 up rows; C = h bf16 [M][N/2],
+                               h = silu(A . Bgate^T) * (A . Bup^T) (a shared expert's
+                               gated MLP step); N % 256 == 0 */
+} moe_gemm_epilogue;
+
+/* C = A . B^T: a bf16 [M][K], b bf16 [N][K] (both K-major, 16-byte aligned),
+ * c [M][N] (or [M][N/2] for MOE_EPI_SWIGLU_BF16), 16-byte aligned.
+ * K % 64 == 0, N % 8 == 0 (MOE_ERR_UNSUPPORTED otherwise); any M. ws: at
+ * least MOE_STATUS_BYTES, its status word records device timeouts. */
+moe_status moe_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int32_t N, int32_t K,
+                         int32_t epilogue, void* c, void* ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/* The router GEMM: logits fp32 [T][E] = x bf16 [T][d_in] . w_router bf16
+ * [E][d_in]^T, the input of moe_route_topk / moe_forward. d_in % 64 == 0,
+ * E % 8 == 0, E <= 1024. */
+moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int32_t T,
+                             int32_t d_in, int32_t E, float* logits, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
 /* Synchronises `stream`, then returns the status recorded in the workspace's
  * status word (MOE_OK if none). */
 moe_status moe_check_device_status(const void* ws, cudaStream_t stream);

@@ -16,6 +16,7 @@ STATUS_BYTES = 256
 OK, INVALID_ARGUMENT, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA, DEVICE_TIMEOUT, DEVICE_BAD_INPUT = range(7)
 GEMM_AUTO, GEMM_TOKEN_TILES, GEMM_WEIGHT_TILES = range(3)
 SCALES_TILED128, SCALES_GROUP32 = range(2)
+EPI_F32, EPI_BF16, EPI_SWIGLU_BF16 = range(3)
 
 
 class MoeError(RuntimeError):
@@ -66,6 +67,8 @@ _SIGS = {
                                              _vp, _vp, _i64, _vp, _sz, _vp]),
     "moe_forward_a4w4": (_i32, [ctypes.POINTER(_Dims), _i32, _vp, _vp, ctypes.POINTER(_Weights),
                                 _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_gemm_bf16": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "moe_router_logits": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "moe_check_device_status": (_i32, [_vp, _vp]),
     "moe_clear_device_status": (_i32, [_vp, _vp]),
     "moe_selftest_wait_timeout": (_i32, [_vp, _sz, ctypes.c_uint32, _vp]),
@@ -233,6 +236,17 @@ def moe_forward_a4w4(T, d, E, k, I, kernel, x, logits, w13, w13_sf, w2, w2_sf, y
     W = _Weights(_ptr(w13), _ptr(w13_sf), _ptr(w2), _ptr(w2_sf))
     _call("moe_forward_a4w4", ctypes.byref(_Dims(T, d, E, k, I)), kernel, _ptr(x), _ptr(logits),
           ctypes.byref(W), _ptr(y), _ptr(topk_ids_out), _ptr(topk_w_out), _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def moe_gemm_bf16(a, b, M, N, K, epilogue, c, ws, stream=None):
+    """C = A . B^T for bf16 a [M][K], b [N][K]; c fp32 / bf16 per the epilogue."""
+    _call("moe_gemm_bf16", _ptr(a), _ptr(b), M, N, K, epilogue, _ptr(c), _ptr(ws),
+          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def moe_router_logits(x, w_router, T, d_in, E, logits, ws, stream=None):
+    _call("moe_router_logits", _ptr(x), _ptr(w_router), T, d_in, E, _ptr(logits), _ptr(ws),
           ws.numel() * ws.element_size(), _stream(stream))
 
 

@@ -348,6 +348,33 @@ moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32
                                        rows_capacity, static_cast<int*>(ws), stream));
 }
 
+moe_status moe_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int32_t N, int32_t K,
+                         int32_t epilogue, void* c, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (epilogue != MOE_EPI_F32 && epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_BF16)
+    return MOE_ERR_UNSUPPORTED;
+  if (K < 64 || K % 64 != 0 || K > (1 << 20) || N < 8 || N % 8 != 0 || N > (1 << 20) ||
+      M >= int64_t(INT32_MAX))
+    return MOE_ERR_UNSUPPORTED;
+  if (epilogue == MOE_EPI_SWIGLU_BF16 && N % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  if (M == 0) return MOE_OK;
+  if (!a || !b || !c || !ws) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c, 16) || !aligned(ws, 4))
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < MOE_STATUS_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(moe::launch_gemm_bf16(a, b, M, N, K, epilogue, c, static_cast<int*>(ws),
+                                         stream));
+}
+
+moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int32_t T,
+                             int32_t d_in, int32_t E, float* logits, void* ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+  if (T < 0 || E < 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (E < 1 || E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  return moe_gemm_bf16(x, w_router, T, E, d_in, MOE_EPI_F32, logits, ws, ws_bytes, stream);
+}
+
 moe_status moe_unpermute_combine(const uint16_t* yp, const int32_t* slot_to_row,
                                  const float* topk_w, int32_t T, int32_t k, int32_t d,
                                  uint16_t* y, cudaStream_t stream) {

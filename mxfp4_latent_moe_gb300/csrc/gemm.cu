@@ -504,11 +504,6 @@ cudaError_t launch_mode(const GemmParams& p, const CUtensorMap& ta, const CUtens
 
 }  // namespace
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 EncodeTiledFn encode_tiled_fn() {
   static EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* ptr = nullptr;

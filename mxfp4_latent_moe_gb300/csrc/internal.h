@@ -41,6 +41,11 @@ cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* coun
 // Shared by the grouped GEMMs: 2-D K-major operand tensor map (dim0 = K
 // inputs, dim1 = rows, 128-input boxes of box_rows rows, 128-byte swizzle;
 // E2M1 operands use TMA's 16U4_ALIGN16B expansion), and the SM count.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();   // cuTensorMapEncodeTiled through the runtime, cached
 bool encode_operand(CUtensorMap* map, const void* base, bool e2m1, int K, int64_t rows,
                     int box_rows);
 bool encode_boxed_weights(CUtensorMap* map, const void* base, int64_t rows, int K);
@@ -55,6 +60,10 @@ cudaError_t launch_gemm_decode_w2(const uint8_t* hq, const uint8_t* hs, const in
                                   const int* offsets, int E, int I, int d, const uint8_t* w2,
                                   const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity,
                                   int* status, cudaStream_t st);
+// Dense BF16 GEMM C = A . B^T (gemm_bf16.cu); epilogues as moe_gemm_epilogue.
+enum GemmEpilogue : int { kEpiF32 = 0, kEpiBf16 = 1, kEpiSwiglu = 2 };
+cudaError_t launch_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int N, int K,
+                             int epilogue, void* c, int* status, cudaStream_t st);
 cudaError_t launch_wait_timeout_selftest(int* status, uint32_t limit_us, cudaStream_t st);
 
 cudaError_t launch_combine(const uint16_t* yp, const int* slot_to_row, const float* w, int T,

@@ -137,6 +137,23 @@ def test_host_validation_rejects_before_any_launch(L):
                None, None, fake, 10 ** 9, None) == abi.UNSUPPORTED               # d % 256
     assert _rc(L, "moe_forward_a4w4", ctypes.byref(dims), 0, fake, fake, ctypes.byref(W), fake,
                None, None, fake, 10, None) == abi.WORKSPACE_TOO_SMALL
+    # BF16 GEMMs: K not a multiple of 64, N not a multiple of 8, SwiGLU N % 256, bad epilogue,
+    # misaligned operands, short workspace, E too large for the router
+    assert _rc(L, "moe_gemm_bf16", fake, fake, 64, 256, 96, 1, fake, fake, 256, None) == \
+        abi.UNSUPPORTED
+    assert _rc(L, "moe_gemm_bf16", fake, fake, 64, 100, 128, 1, fake, fake, 256, None) == \
+        abi.UNSUPPORTED
+    assert _rc(L, "moe_gemm_bf16", fake, fake, 64, 384, 128, 2, fake, fake, 256, None) == \
+        abi.UNSUPPORTED
+    assert _rc(L, "moe_gemm_bf16", fake, fake, 64, 256, 128, 3, fake, fake, 256, None) == \
+        abi.UNSUPPORTED
+    assert _rc(L, "moe_gemm_bf16", ctypes.c_void_p(4104), fake, 64, 256, 128, 1, fake, fake, 256,
+               None) == abi.INVALID_ARGUMENT
+    assert _rc(L, "moe_gemm_bf16", fake, fake, 64, 256, 128, 1, fake, fake, 8, None) == \
+        abi.WORKSPACE_TOO_SMALL
+    assert _rc(L, "moe_gemm_bf16", fake, fake, 0, 256, 128, 1, None, None, 0, None) == abi.OK
+    assert _rc(L, "moe_router_logits", fake, fake, 4, 7168, 2048, fake, fake, 256, None) == \
+        abi.UNSUPPORTED
     # status helpers
     assert _rc(L, "moe_check_device_status", None, None) == abi.INVALID_ARGUMENT
     assert _rc(L, "moe_selftest_wait_timeout", fake, 8, 100, None) == abi.WORKSPACE_TOO_SMALL
