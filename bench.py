@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--cpu-sample", type=int, default=0, help="oracle tokens (0 = automatic)")
     ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "token", "weight"],
                     help="grouped-GEMM family (auto = the library's default for the shape)")
+    ap.add_argument("--step", default="", choices=["", "router", "latent_down", "latent_up",
+                                                   "shared_experts"],
+                    help="time one neighbouring BF16 step at the workload's T instead of the layer")
     ap.add_argument("--a4w4", action="store_true",
                     help="MXFP4 stage-1 activations (moe_forward_a4w4); the family is stage 2's")
     return ap.parse_args()
@@ -219,12 +222,119 @@ def run_reference(args, wl):
     print(json.dumps(line))
 
 
+# The neighbouring BF16 steps at the layer's sizes: (name, [(N, K, epilogue)] per GEMM call),
+# hidden 7,168, latent 3,584, 896 experts; shared experts: 2 x (7,168 -> 3,072 -> 7,168).
+HIDDEN, LATENT, SHARED_I, N_SHARED = 7168, 3584, 3072, 2
+BF16_STEPS = {
+    "router": [(896, HIDDEN, 0)],
+    "latent_down": [(LATENT, HIDDEN, 1)],
+    "latent_up": [(HIDDEN, LATENT, 1)],
+    "shared_experts": [(2 * SHARED_I, HIDDEN, 2), (HIDDEN, SHARED_I, 1)] * N_SHARED,
+}
+
+
+def run_step(args, wl):
+    """Times one neighbouring BF16 step (moe_gemm_bf16 calls) on T tokens."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_latent_moe_gb300 import abi
+    dev = torch.device("cuda", 0)
+    T = wl.T
+    calls = BF16_STEPS[args.step]
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    bufs = []
+    for i, (N, K, epi) in enumerate(calls):
+        a_rows = T
+        a = (torch.randn(a_rows, K, generator=g, device=dev)).to(torch.bfloat16)
+        b = (torch.randn(N, K, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        n_out = N // 2 if epi == 2 else N
+        c = torch.empty(T, n_out, dtype=torch.float32 if epi == 0 else torch.bfloat16, device=dev)
+        bufs.append((a, b, c, N, K, epi))
+    ws = torch.zeros(max(abi.moe_gemm_bf16_workspace_size(T, N, K, epi)
+                         for _, _, _, N, K, epi in bufs), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        for a, b, c, N, K, epi in bufs:
+            abi.moe_gemm_bf16(a, b, T, N, K, epi, c, ws)
+
+    sampler = ClockSampler(0)
+    sampler.start()
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    sampler.mark()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[2 * i].record(stream)
+        step()
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    if abi.moe_check_device_status(ws) != abi.OK:
+        raise RuntimeError("device status error")
+    total_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps))
+    ms = total_ms / args.steps
+    flops = sum(2.0 * T * N * K for _, _, _, N, K, _ in bufs)
+    w_bytes = sum(N * K * 2 for _, _, _, N, K, _ in bufs)
+    io_bytes = sum(T * K * 2 + T * (N // 2 if epi == 2 else N) * (4 if epi == 0 else 2)
+                   for _, _, _, N, K, epi in bufs)
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    t_mem = (w_bytes + io_bytes) / (hbm * 1e9)
+    t_math = flops / (bf16 * 1e12)
+    bound = "hbm" if t_mem >= t_math else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": (w_bytes + io_bytes) / (ms / 1e3) / 1e9, "peak": hbm,
+                "unit": "GB/s", "algorithmic_bytes": w_bytes + io_bytes}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / (ms / 1e3) / 1e12, "peak": bf16,
+                "unit": "TFLOP/s", "algorithmic_flops": flops}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = peak_src
+    roof["traffic"] = None
+    # oracle on a bounded sample of rows
+    import oracle
+    oracle.build_oracle()
+    n = 2
+    t0 = time.perf_counter()
+    for a, b, c, N, K, epi in bufs:
+        ab = a[:n].cpu().view(torch.int16).numpy().view("uint16")
+        bb = b.cpu().view(torch.int16).numpy().view("uint16")
+        (oracle.gemm_bf16_swiglu if epi == 2 else oracle.gemm_bf16)(ab, bb)
+    dt = time.perf_counter() - t0
+    splits = [abi.moe_gemm_bf16_workspace_size(T, N, K, epi) > 256 for _, _, _, N, K, epi in bufs]
+    line = {
+        "metric": "BF16 %s step tokens/s (neighbouring step of the MoE layer), 1xGB300" % args.step,
+        "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16xbf16->f32", "data": "synthetic (seeded N(0,1) "
+        "activations, N(0,0.02) weights)",
+        "config": {"workload": "%s_t%d" % (args.step, T), "T": T,
+                   "gemms": [[N, K, ["f32", "bf16", "swiglu_bf16"][epi]] for _, _, _, N, K, epi in bufs],
+                   "split_k": splits,
+                   "l2": "L2 flushed between steps (256 MB write)"},
+        "roofline": roof, "gpu_launches": (len(bufs) + sum(splits)) * args.steps,
+        "tflops": flops / (ms / 1e3) / 1e12,
+        "cpu_baseline": {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d tokens, all GEMMs of the step (%.1f s)" % (n, dt)},
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
     from mxfp4_latent_moe_gb300 import synth
     wl = synth.workload(args.workload) if args.tokens <= 0 else synth.full_dims(args.tokens)
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.step:
+        return run_step(args, wl)
 
     import torch
     from mxfp4_latent_moe_gb300 import replicas

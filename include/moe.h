@@ -356,15 +356,22 @@ typedef enum {
 
 /* C = A . B^T: a bf16 [M][K], b bf16 [N][K] (both K-major, 16-byte aligned),
  * c [M][N] (or [M][N/2] for MOE_EPI_SWIGLU_BF16), 16-byte aligned.
- * K % 64 == 0, N % 8 == 0 (MOE_ERR_UNSUPPORTED otherwise); any M. ws: at
- * least MOE_STATUS_BYTES, its status word records device timeouts. */
+ * K % 64 == 0, N % 8 == 0 (MOE_ERR_UNSUPPORTED otherwise); any M.
+ * ws (16-byte aligned): moe_gemm_bf16_workspace_size bytes; its status word
+ * records device timeouts, and calls with few output tiles (small M) split K
+ * over the SMs and keep fp32 partial sums there, added in a fixed order, so
+ * the result does not depend on the split. */
 moe_status moe_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int32_t N, int32_t K,
                          int32_t epilogue, void* c, void* ws, size_t ws_bytes,
                          cudaStream_t stream);
 
+/* Workspace bytes of moe_gemm_bf16 for this shape (0 for an unsupported one). */
+size_t moe_gemm_bf16_workspace_size(int64_t M, int32_t N, int32_t K, int32_t epilogue);
+
 /* The router GEMM: logits fp32 [T][E] = x bf16 [T][d_in] . w_router bf16
  * [E][d_in]^T, the input of moe_route_topk / moe_forward. d_in % 64 == 0,
- * E % 8 == 0, E <= 1024. */
+ * E % 8 == 0, E <= 1024; ws: moe_gemm_bf16_workspace_size(T, E, d_in,
+ * MOE_EPI_F32) bytes. */
 moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int32_t T,
                              int32_t d_in, int32_t E, float* logits, void* ws, size_t ws_bytes,
                              cudaStream_t stream);

@@ -69,6 +69,7 @@ _SIGS = {
                                 _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_gemm_bf16": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "moe_router_logits": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "moe_gemm_bf16_workspace_size": (_sz, [_i64, _i32, _i32, _i32]),
     "moe_check_device_status": (_i32, [_vp, _vp]),
     "moe_clear_device_status": (_i32, [_vp, _vp]),
     "moe_selftest_wait_timeout": (_i32, [_vp, _sz, ctypes.c_uint32, _vp]),
@@ -243,6 +244,10 @@ def moe_gemm_bf16(a, b, M, N, K, epilogue, c, ws, stream=None):
     """C = A . B^T for bf16 a [M][K], b [N][K]; c fp32 / bf16 per the epilogue."""
     _call("moe_gemm_bf16", _ptr(a), _ptr(b), M, N, K, epilogue, _ptr(c), _ptr(ws),
           ws.numel() * ws.element_size(), _stream(stream))
+
+
+def moe_gemm_bf16_workspace_size(M, N, K, epilogue):
+    return lib().moe_gemm_bf16_workspace_size(M, N, K, epilogue)
 
 
 def moe_router_logits(x, w_router, T, d_in, E, logits, ws, stream=None):

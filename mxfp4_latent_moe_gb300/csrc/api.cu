@@ -360,11 +360,20 @@ moe_status moe_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int32_
   if (epilogue == MOE_EPI_SWIGLU_BF16 && N % 256 != 0) return MOE_ERR_UNSUPPORTED;
   if (M == 0) return MOE_OK;
   if (!a || !b || !c || !ws) return MOE_ERR_INVALID_ARGUMENT;
-  if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c, 16) || !aligned(ws, 4))
+  if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c, 16) || !aligned(ws, 16))
     return MOE_ERR_INVALID_ARGUMENT;
-  if (ws_bytes < MOE_STATUS_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  return from_cuda(moe::launch_gemm_bf16(a, b, M, N, K, epilogue, c, static_cast<int*>(ws),
-                                         stream));
+  if (ws_bytes < MOE_STATUS_BYTES + moe::bf16_partial_bytes(M, N, K, epilogue))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(moe::launch_gemm_bf16(a, b, M, N, K, epilogue, c,
+                                         at<float>(ws, MOE_STATUS_BYTES),
+                                         static_cast<int*>(ws), stream));
+}
+
+size_t moe_gemm_bf16_workspace_size(int64_t M, int32_t N, int32_t K, int32_t epilogue) {
+  if (M < 0 || N < 8 || N % 8 != 0 || K < 64 || K % 64 != 0) return 0;
+  if (epilogue != MOE_EPI_F32 && epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_BF16)
+    return 0;
+  return MOE_STATUS_BYTES + moe::bf16_partial_bytes(M, N, K, epilogue);
 }
 
 moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int32_t T,

@@ -20,6 +20,10 @@
 // run in groups of 8 row tiles with the row tile fastest, so the CTAs in
 // flight share B tiles and keep a bounded slice of A in L2. Rows of A and B
 // past M and N are zero-filled by TMA; stores past M and N are skipped.
+// Calls with too few tiles to cover the GPU (decode: one row tile) split K:
+// each CTA accumulates one K-slice of a tile and writes its fp32 partial sums
+// to the workspace; a second kernel adds the slices in a fixed order and
+// applies the epilogue, so results do not depend on the split.
 // Every wait is bounded (MOE_ERR_DEVICE_TIMEOUT in the status word).
 #include "internal.h"
 
@@ -68,7 +72,10 @@ struct Bf16Params {
   int N;          // rows of B
   int K;
   int MT, NT;     // row tiles of A; column tiles of C (EPI kEpiSwiglu: of h)
+  int KS;         // K-slices per tile (1: no split)
+  int KTS;        // 64-input stages per slice
   void* c;
+  float* partial; // KS > 1: fp32 [KS][M][N] partial sums
   int* status;
 };
 
@@ -103,8 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KT = p.K / BKB;
-  const int total = p.MT * p.NT;
+  const int KT = p.KTS;
+  const int total = p.MT * p.NT * p.KS;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -134,10 +141,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0;
     uint32_t filled = 0, last_parity = 0;
     bool failed = false;
-    for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
+    for (int work = blockIdx.x; work < total && !failed; work += gridDim.x) {
       int mt, nt;
-      bf16_tile(tile, p.MT, p.NT, mt, nt);
-      for (int kt = 0; kt < KT; ++kt) {
+      bf16_tile(work / p.KS, p.MT, p.NT, mt, nt);
+      const int k0 = (work % p.KS) * KT;   // first stage of this K-slice
+      for (int kt = k0; kt < k0 + KT; ++kt) {
         if (!mbar_wait_warp(&empty[stage], phase ^ 1u, abort_flag)) {
           failed = true;
           break;
@@ -179,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0, acc_phases = 0;
     int buf = 0;
     bool failed = false;
-    for (int tile = blockIdx.x; tile < total && !failed; tile += gridDim.x) {
+    for (int work = blockIdx.x; work < total && !failed; work += gridDim.x) {
       if (!mbar_wait_warp(&acc_empty[buf], ((acc_phases >> buf) & 1u) ^ 1u, abort_flag)) {
         failed = true;
         break;
@@ -229,9 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;
     uint32_t acc_phases = 0;
     int buf = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int work = blockIdx.x; work < total; work += gridDim.x) {
       int mt, nt;
-      bf16_tile(tile, p.MT, p.NT, mt, nt);
+      bf16_tile(work / p.KS, p.MT, p.NT, mt, nt);
+      const int ks = work % p.KS;
       bool ok = mbar_wait(&acc_full[buf], (acc_phases >> buf) & 1u, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -259,6 +268,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       buf ^= 1;
       const int64_t row = int64_t(mt) * BM + q * 32 + lane;
       if (row >= p.M) continue;
+      if (p.KS > 1) {   // raw fp32 sums of this K-slice, in C's column order over all N rows of B
+        float* dst = p.partial + (int64_t(ks) * p.M + row) * p.N;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          // columns of v[c]: swiglu gate (c < 2) / up (c >= 2) halves, else 128 half + 32 c
+          const int colc = EPI == kEpiSwiglu
+                               ? (c < 2 ? nt * 128 + 64 * half + 32 * c
+                                        : (p.N >> 1) + nt * 128 + 64 * half + 32 * (c - 2))
+                               : nt * BN + 128 * half + 32 * c;
+#pragma unroll
+          for (int w = 0; w < 8; ++w)
+            if (colc + 4 * w < p.N)
+              reinterpret_cast<uint4*>(dst + colc)[w] =
+                  make_uint4(v[c][4 * w], v[c][4 * w + 1], v[c][4 * w + 2], v[c][4 * w + 3]);
+        }
+        continue;
+      }
       if (EPI == kEpiSwiglu) {
         const int Nh = p.N >> 1;
         uint16_t* dst = static_cast<uint16_t*>(p.c) + row * Nh + int64_t(nt) * 128 + 64 * half;
@@ -314,6 +340,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+// Sum of the K-slices in slice order, then the epilogue; thread = 4 outputs.
+template <int EPI>
+__global__ void __launch_bounds__(256)
+    bf16_splitk_reduce_kernel(const float* __restrict__ partial, int KS, int64_t M, int N,
+                              void* __restrict__ c) {
+  const int n_out = EPI == kEpiSwiglu ? (N >> 1) : N;
+  const int64_t g = int64_t(blockIdx.x) * 256 + threadIdx.x;   // group of 4 outputs
+  const int64_t per_row = n_out >> 2;
+  if (g >= M * per_row) return;
+  const int64_t row = g / per_row;
+  const int col = int(g - row * per_row) * 4;
+  const int64_t slice = M * int64_t(N);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, up[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < KS; ++s) {
+    const float4 a = *reinterpret_cast<const float4*>(partial + s * slice + row * N + col);
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    if (EPI == kEpiSwiglu) {
+      const float4 u = *reinterpret_cast<const float4*>(partial + s * slice + row * N + (N >> 1) + col);
+      up[0] += u.x; up[1] += u.y; up[2] += u.z; up[3] += u.w;
+    }
+  }
+  if (EPI == kEpiF32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(c) + row * N + col) =
+        make_float4(acc[0], acc[1], acc[2], acc[3]);
+    return;
+  }
+  if (EPI == kEpiSwiglu) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = __fdividef(acc[i] * up[i], 1.0f + __expf(-acc[i]));
+  }
+  *reinterpret_cast<uint2*>(static_cast<uint16_t*>(c) + row * n_out + col) =
+      make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+}
+
 // bf16 [rows][K] K-major operand: boxes of 64 inputs (128 bytes) x box_rows,
 // 128-byte swizzle, rows past the end zero-filled.
 bool encode_bf16(CUtensorMap* map, const void* base, int K, int64_t rows, int box_rows) {
@@ -331,24 +391,65 @@ bool encode_bf16(CUtensorMap* map, const void* base, int K, int64_t rows, int bo
 }
 
 template <int EPI>
+cudaError_t launch_epi_main(const Bf16Params& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                            cudaStream_t st);
+
+template <int EPI>
 cudaError_t launch_epi(const Bf16Params& p, const CUtensorMap& ta, const CUtensorMap& tb,
                        cudaStream_t st) {
+  if (p.KS > 1) {
+    cudaError_t err = launch_epi_main<EPI>(p, ta, tb, st);
+    if (err != cudaSuccess) return err;
+    const int n_out = EPI == kEpiSwiglu ? (p.N >> 1) : p.N;
+    const int64_t groups = p.M * (n_out / 4);
+    bf16_splitk_reduce_kernel<EPI><<<dim3(unsigned((groups + 255) / 256)), 256, 0, st>>>(
+        p.partial, p.KS, p.M, p.N, p.c);
+    return cudaGetLastError();
+  }
+  return launch_epi_main<EPI>(p, ta, tb, st);
+}
+
+template <int EPI>
+cudaError_t launch_epi_main(const Bf16Params& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                            cudaStream_t st) {
   cudaError_t err = cudaFuncSetAttribute(gemm_bf16_kernel<EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
   if (err != cudaSuccess) return err;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  const int64_t tiles = int64_t(p.MT) * p.NT;
-  const int grid = int(tiles < sms ? tiles : sms);
+  const int64_t work = int64_t(p.MT) * p.NT * p.KS;
+  const int grid = int(work < sms ? work : sms);
   gemm_bf16_kernel<EPI><<<grid, kThreads, kSmemBytes, st>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+// K-slices for a call: 1 unless the tiles cover less than half of the 152
+// SMs; then as many equal slices as fit one wave of 152 CTAs, each at least 4
+// stages long. Depends only on the shape, so the workspace size can be stated
+// before the call.
+int bf16_k_splits(int64_t M, int N, int K, int epilogue) {
+  const int64_t MT = (M + BM - 1) / BM;
+  const int64_t NT = epilogue == kEpiSwiglu ? (N / 2) / 128 : (N + BN - 1) / BN;
+  const int64_t tiles = MT * NT;
+  const int KT = K / BKB;
+  if (tiles >= 76 || KT < 8) return 1;
+  int ks = int(152 / tiles);
+  ks = ks < KT / 4 ? ks : KT / 4;
+  ks = ks < 32 ? ks : 32;
+  while (ks > 1 && KT % ks != 0) --ks;   // equal slices
+  return ks > 1 ? ks : 1;
+}
+
+size_t bf16_partial_bytes(int64_t M, int N, int K, int epilogue) {
+  const int ks = bf16_k_splits(M, N, K, epilogue);
+  return ks > 1 ? size_t(ks) * size_t(M) * size_t(N) * 4 : 0;
+}
+
 cudaError_t launch_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int N, int K,
-                             int epilogue, void* c, int* status, cudaStream_t st) {
+                             int epilogue, void* c, float* partial, int* status, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
   CUtensorMap ta, tb;
   if (!encode_bf16(&ta, a, K, M, BM)) return cudaErrorInvalidValue;
@@ -359,6 +460,9 @@ cudaError_t launch_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, in
   p.K = K;
   p.MT = int((M + BM - 1) / BM);
   p.NT = epilogue == kEpiSwiglu ? (N / 2) / 128 : (N + BN - 1) / BN;
+  p.KS = bf16_k_splits(M, N, K, epilogue);
+  p.KTS = (K / BKB) / p.KS;
+  p.partial = partial;
   p.c = c;
   p.status = status;
   if (epilogue == kEpiF32) return launch_epi<kEpiF32>(p, ta, tb, st);

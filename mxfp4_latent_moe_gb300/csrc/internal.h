@@ -62,8 +62,10 @@ cudaError_t launch_gemm_decode_w2(const uint8_t* hq, const uint8_t* hs, const in
                                   int* status, cudaStream_t st);
 // Dense BF16 GEMM C = A . B^T (gemm_bf16.cu); epilogues as moe_gemm_epilogue.
 enum GemmEpilogue : int { kEpiF32 = 0, kEpiBf16 = 1, kEpiSwiglu = 2 };
+int bf16_k_splits(int64_t M, int N, int K, int epilogue);
+size_t bf16_partial_bytes(int64_t M, int N, int K, int epilogue);   // 0 without a split
 cudaError_t launch_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int N, int K,
-                             int epilogue, void* c, int* status, cudaStream_t st);
+                             int epilogue, void* c, float* partial, int* status, cudaStream_t st);
 cudaError_t launch_wait_timeout_selftest(int* status, uint32_t limit_us, cudaStream_t st);
 
 cudaError_t launch_combine(const uint16_t* yp, const int* slot_to_row, const float* w, int T,

@@ -5,7 +5,8 @@ Bars (fp32 accumulation of bf16 products, then the output rounding):
   fp32 out:  |gpu - ref| <= 1e-5 * sum_k |a_k b_k| + 1e-30
   bf16 out:  |gpu - ref| <= 2^-8 * |ref| + 1e-5 * sum_k |a_k b_k| + 1e-30
 Shapes cover ragged M and N tails, several raster groups, K from one stage
-to many, the router at the layer's sizes, and the SwiGLU epilogue.
+to many, calls that split K over the SMs (few tiles) and calls that do not,
+the router at the layer's sizes, and the SwiGLU epilogue.
 """
 import numpy as np
 import pytest
@@ -46,7 +47,8 @@ def _absdot(a, b):
 def test_gemm_bf16_matches_oracle(abi, orc, M, N, K, epi):
     a, b = _operands(M, N, K, seed=M + N + K)
     c = torch.full((M, N), 7.0, dtype=torch.float32 if epi == 0 else torch.bfloat16, device="cuda")
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(abi.moe_gemm_bf16_workspace_size(M, N, K, epi), dtype=torch.uint8,
+                     device="cuda")
     abi.moe_gemm_bf16(a.cuda(), b.cuda(), M, N, K, epi, c, ws)
     assert abi.moe_check_device_status(ws) == 0
     ref = orc.gemm_bf16(_bits(a), _bits(b))
@@ -61,7 +63,8 @@ def test_gemm_bf16_matches_oracle(abi, orc, M, N, K, epi):
 def test_gemm_bf16_swiglu_matches_oracle(abi, orc, M, Nh, K):
     a, b = _operands(M, 2 * Nh, K, seed=M + Nh, scale_b=0.02)
     h = torch.full((M, Nh), 7.0, dtype=torch.bfloat16, device="cuda")
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(abi.moe_gemm_bf16_workspace_size(M, 2 * Nh, K, 2), dtype=torch.uint8,
+                     device="cuda")
     abi.moe_gemm_bf16(a.cuda(), b.cuda(), M, 2 * Nh, K, 2, h, ws)
     assert abi.moe_check_device_status(ws) == 0
     ref = orc.gemm_bf16_swiglu(_bits(a), _bits(b))
@@ -82,7 +85,8 @@ def test_router_logits_feed_the_routing(abi, orc, T):
     d_in, E, k = 7168, 896, 16
     x, w = _operands(T, E, d_in, seed=T, scale_b=0.02)
     logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(abi.moe_gemm_bf16_workspace_size(T, E, d_in, 0), dtype=torch.uint8,
+                     device="cuda")
     abi.moe_router_logits(x.cuda(), w.cuda(), T, d_in, E, logits, ws)
     assert abi.moe_check_device_status(ws) == 0
     ref = orc.gemm_bf16(_bits(x), _bits(w))
