@@ -13,6 +13,7 @@
 //   2. permute_scan:    counts, padded offsets, chunk bases (exclusive over c)
 //   3. permute_scatter: row = offsets[e] + base[c][e] + rank
 // row_to_slot is set to -1 by a memset before the scatter fills the used rows.
+// A batch of one chunk (T <= 256, decode) runs all of it in one block.
 #include <mutex>
 
 #include "internal.h"
@@ -127,6 +128,80 @@ __global__ void __launch_bounds__(kChunk) permute_scatter_kernel(
   }
 }
 
+// Batches of one chunk (T <= 256, decode): histogram, scan and scatter in
+// one block, row_to_slot filled with -1 first (one launch instead of three
+// and a memset). Same masks and ranks as the three kernels above.
+__global__ void __launch_bounds__(kChunk)
+    permute_single_kernel(const int* __restrict__ ids, int T, int E, int k, int pad_m,
+                          int* __restrict__ counts, int* __restrict__ offsets,
+                          int* __restrict__ slot_to_row, int* __restrict__ row_to_slot,
+                          int64_t rows_capacity, int* status) {
+  extern __shared__ uint32_t masks[];            // [kWarps][E], then offsets [E+1]
+  int* off_s = reinterpret_cast<int*>(masks + kWarps * E);
+  __shared__ int warp_sums[kWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    int64_t done = 0;
+    if ((reinterpret_cast<uintptr_t>(row_to_slot) & 15u) == 0) {
+      int4* r4 = reinterpret_cast<int4*>(row_to_slot);
+      for (int64_t i = tid; i < rows_capacity / 4; i += kChunk) r4[i] = make_int4(-1, -1, -1, -1);
+      done = (rows_capacity / 4) * 4;
+    }
+    for (int64_t i = done + tid; i < rows_capacity; i += kChunk) row_to_slot[i] = -1;
+  }
+  build_masks(ids, T, E, k, masks, status);      // ends with __syncthreads
+  // experts 4 tid .. 4 tid + 3: counts, padded sizes, block-wide exclusive scan
+  int cnt[4], pad[4], sum = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = 4 * tid + q;
+    cnt[q] = 0;
+    if (e < E)
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) cnt[q] += __popc(masks[w * E + e]);
+    pad[q] = (cnt[q] + pad_m - 1) / pad_m * pad_m;
+    sum += pad[q];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += n;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int base = incl - sum;
+  for (int w = 0; w < warp; ++w) base += warp_sums[w];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = 4 * tid + q;
+    if (e < E) {
+      counts[e] = cnt[q];
+      offsets[e] = base;
+      off_s[e] = base;
+      if (e == E - 1) {
+        offsets[E] = base + pad[q];
+        off_s[E] = base + pad[q];
+      }
+    }
+    base += pad[q];
+  }
+  __syncthreads();
+  const int t = tid;
+  if (t >= T) return;
+  const uint32_t lower = (1u << lane) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const int e = ids[int64_t(t) * k + j];
+    if (e < 0 || e >= E) continue;
+    int rank = __popc(masks[warp * E + e] & lower);
+    for (int w = 0; w < warp; ++w) rank += __popc(masks[w * E + e]);
+    const int row = off_s[e] + rank;
+    const int slot = t * k + j;
+    slot_to_row[slot] = row;
+    row_to_slot[row] = slot;
+  }
+}
+
 }  // namespace
 
 size_t permute_scratch_bytes(int T, int E) {
@@ -139,6 +214,11 @@ cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* 
                            int64_t rows_capacity, int* hist, int* status, cudaStream_t st) {
   const int C = (T + kChunk - 1) / kChunk;
   const size_t smem = size_t(kWarps) * E * sizeof(uint32_t);
+  if (C == 1 && row_to_slot) {   // one chunk: a single launch
+    permute_single_kernel<<<1, kChunk, smem + size_t(E + 1) * sizeof(int), st>>>(
+        ids, T, E, k, pad_m, counts, offsets, slot_to_row, row_to_slot, rows_capacity, status);
+    return cudaGetLastError();
+  }
   if (C > 0 && k > 0) {
     permute_count_kernel<<<C, kChunk, smem, st>>>(ids, T, E, k, hist, status);
     cudaError_t err = cudaGetLastError();

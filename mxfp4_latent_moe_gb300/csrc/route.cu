@@ -6,9 +6,10 @@
 // weights are sigmoid(l_j) / sum of the k selected sigmoids.
 //
 // Each lane holds the logits of experts lane, lane+32, ... (up to 32 per lane
-// for E <= 1024) in registers. k rounds of a warp-wide (value desc, id asc)
-// arg-max by butterfly shuffles pick the experts in output order; the winner's
-// owner lane marks it taken. Reads are coalesced: a token's row is read once.
+// for E <= 1024) in registers and keeps its two best untaken ones. k rounds
+// of a warp-wide (value desc, id asc) arg-max of the lanes' heads by
+// butterfly shuffles pick the experts in output order. Reads are coalesced: a
+// token's row is read once.
 #include "internal.h"
 
 namespace moe {
@@ -19,6 +20,31 @@ constexpr int kWarpsPerBlock = 8;
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
+}
+
+// The lane's best two values (by `better`) among those worse than (lv, li)
+// when `limit`, else among all of its values; sentinels (-inf, INT_MAX) fill.
+template <int NPL>
+__device__ __forceinline__ void lane_top2(const float (&v)[NPL], int E, int lane, bool limit,
+                                          float lv, int li, float& av, int& ai, float& bv,
+                                          int& bi) {
+  av = bv = -INFINITY;
+  ai = bi = 0x7FFFFFFF;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && (!limit || better(lv, li, v[i], e)) && better(v[i], e, bv, bi)) {
+      if (better(v[i], e, av, ai)) {
+        bv = av;
+        bi = ai;
+        av = v[i];
+        ai = e;
+      } else {
+        bv = v[i];
+        bi = e;
+      }
+    }
+  }
 }
 
 template <int NPL>
@@ -35,33 +61,39 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int e = lane + 32 * i;
     v[i] = e < E ? __ldg(row + e) : -INFINITY;
   }
-  uint32_t taken = 0;
+  // Each lane keeps its two best untaken values; a round is a warp arg-max of
+  // the lanes' heads (value desc, id asc) and a pop on the winning lane. The
+  // values a lane has given up are always its best ones, so once its two are
+  // gone it rescans for the best two below its last pick.
+  float av, bv;
+  int ai, bi;
+  lane_top2<NPL>(v, E, lane, false, 0.0f, 0, av, ai, bv, bi);
   float my_v = 0.0f;
   int my_id = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
-        bv = v[i];
-        bi = e;
-      }
-    }
+    float wv = av;
+    int wi = ai;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
+      const float ov = __shfl_xor_sync(0xffffffffu, wv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, wi, off);
+      if (better(ov, oi, wv, wi)) {
+        wv = ov;
+        wi = oi;
       }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if ((wi & 31) == lane) {   // this lane's head won: pop it
+      const float lv = av;
+      const int li = ai;
+      av = bv;
+      ai = bi;
+      bv = -INFINITY;
+      bi = 0x7FFFFFFF;
+      if (ai == 0x7FFFFFFF) lane_top2<NPL>(v, E, lane, true, lv, li, av, ai, bv, bi);
+    }
     if (lane == j) {
-      my_v = bv;
-      my_id = bi;
+      my_v = wv;
+      my_id = wi;
     }
   }
   // sigmoid of the selected logits, renormalised over the k of them

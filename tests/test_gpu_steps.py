@@ -38,6 +38,21 @@ def test_route_bit_exact(abi, orc, T, E, k):
     np.testing.assert_allclose(w, rw, rtol=2e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("lane_of_top", [0, 5, 31])
+def test_route_top_experts_in_one_lane(abi, orc, lane_of_top):
+    """All of the largest logits on experts e = lane (mod 32): the lane that
+    holds them gives up every pick, so it rescans its values many times."""
+    rng = np.random.default_rng(lane_of_top)
+    T, E, k = 96, 896, 16
+    logits = rng.normal(0, 1, (T, E)).astype(np.float32)
+    logits[:, lane_of_top::32] += 10.0
+    logits[::4, lane_of_top::64] = 20.0                        # ties inside that lane too
+    ids, w = _route_gpu(abi, logits, k)
+    rids, rw = orc.route_topk(logits, k)
+    assert np.array_equal(ids, rids)
+    np.testing.assert_allclose(w, rw, rtol=2e-6, atol=1e-7)
+
+
 def test_route_ties_signed_zero_and_saturation(abi, orc):
     rng = np.random.default_rng(11)
     T, E, k = 512, 896, 16
@@ -69,7 +84,8 @@ def _permute_gpu(abi, ids, E, pad_m, rows_capacity=None):
 
 
 @pytest.mark.parametrize("pad_m", [1, 16, 128])
-@pytest.mark.parametrize("T,E,k", [(1000, 896, 16), (64, 896, 16), (513, 64, 8), (1, 5, 2)])
+@pytest.mark.parametrize("T,E,k", [(1000, 896, 16), (64, 896, 16), (513, 64, 8), (1, 5, 2),
+                                   (256, 1024, 32), (257, 896, 16)])
 def test_permute_bit_exact(abi, orc, T, E, k, pad_m):
     rng = np.random.default_rng(T * 7 + pad_m)
     ids, _ = orc.route_topk(rng.normal(0, 1, (T, E)).astype(np.float32), k)
@@ -80,6 +96,7 @@ def test_permute_bit_exact(abi, orc, T, E, k, pad_m):
         assert np.array_equal(got[key], ref[key]), key
     n = int(ref["offsets"][-1])
     assert np.array_equal(got["row_to_slot"][:n], ref["row_to_slot"])
+    assert np.all(got["row_to_slot"][n:] == -1)            # rows past the groups hold no slot
 
 
 def test_permute_one_hot_expert_and_empty_experts(abi, orc):
