@@ -31,11 +31,10 @@
 // Tiles are (expert, n-tile, m-tile) with the m-tile fastest, so CTAs running
 // at the same time share one expert's weight tile through L2. The expert row
 // offsets are read on the device: no host synchronisation.
-// Stage 1 runs as 2-CTA clusters: the pair takes n-tiles 2j and 2j + 1 of one
-// (expert, m-tile), each CTA loads one 64-row half of the A tile and
+// Both stages run as 2-CTA clusters: the pair takes n-tiles 2j and 2j + 1 of
+// one (expert, m-tile), each CTA loads one 64-row half of the A tile and
 // multicasts it to both, so the activations cross from L2 once per pair
-// (about 10% faster stage 1 on prefill; stage 2 measured no gain and runs
-// one CTA per tile).
+// (on prefill about 10% faster stage 1 and 3-5% faster stage 2).
 // Every wait is bounded; on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT,
 // drains its outstanding copies and tensor-core work, frees tensor memory and
 // exits.
@@ -570,17 +569,14 @@ __global__ void wait_timeout_selftest_kernel(int* status, uint64_t limit_ns) {
   }
 }
 
-// CTAs per cluster of the token-tile GEMMs: stage 1 runs in A-tile pairs;
-// stage 2 (bf16 output tiles) ran slower paired and stays one CTA per tile.
-template <int MODE>
-constexpr int pair_cl() {
-  return MODE == 0 ? 2 : 1;
-}
+// CTAs per cluster of the token-tile GEMMs (2: A-tile pairs; 1 runs the same
+// kernel one CTA per tile)
+constexpr int kPairCL = 2;
 
 template <int MODE, bool A4 = false, int HSL = kScalesTiled128>
 cudaError_t launch_mode(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                         cudaStream_t st) {
-  constexpr int CL = pair_cl<MODE>();
+  constexpr int CL = kPairCL;
   auto kernel = grouped_gemm_kernel<MODE, A4, HSL, CL>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
@@ -695,7 +691,7 @@ cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int*
                                 const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
                                 int64_t rows_capacity, int* status, cudaStream_t st) {
   CUtensorMap ta, tb;
-  if (!encode_operand(&ta, xq, false, d, rows_capacity, BM / pair_cl<0>()))
+  if (!encode_operand(&ta, xq, false, d, rows_capacity, BM / kPairCL))
     return cudaErrorInvalidValue;
   if (!encode_boxed_weights(&tb, w13, int64_t(E) * 2 * I, d)) return cudaErrorInvalidValue;
   GemmParams p{};
@@ -722,7 +718,7 @@ cudaError_t launch_gemm_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs, const
                                      cudaStream_t st) {
   CUtensorMap ta, tb;
   // packed activations: d/2 bytes per row, 128-byte boxes of 128 rows
-  if (!encode_operand(&ta, xq, false, d / 2, rows_capacity, BM / pair_cl<0>()))
+  if (!encode_operand(&ta, xq, false, d / 2, rows_capacity, BM / kPairCL))
     return cudaErrorInvalidValue;
   if (!encode_boxed_weights_packed(&tb, w13, int64_t(E) * 2 * I, d)) return cudaErrorInvalidValue;
   GemmParams p{};
@@ -748,7 +744,7 @@ cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* coun
                            const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity, int* status,
                            cudaStream_t st) {
   CUtensorMap ta, tb;
-  if (!encode_operand(&ta, hq, false, I, rows_capacity, BM / pair_cl<1>()))
+  if (!encode_operand(&ta, hq, false, I, rows_capacity, BM / kPairCL))
     return cudaErrorInvalidValue;
   if (!encode_boxed_weights(&tb, w2, int64_t(E) * d, I)) return cudaErrorInvalidValue;
   GemmParams p{};
