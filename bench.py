@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -171,6 +172,28 @@ def oracle_inputs(L, n_tokens):
     return xb, lg, W
 
 
+def cpu_model():
+    """The host CPU's name (x86 `model name`; Arm implementer/part codes)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+    except OSError:
+        return platform.machine()
+    for line in info:
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    fields = {}
+    for line in info:
+        if ":" in line:
+            key, val = (x.strip() for x in line.split(":", 1))
+            fields.setdefault(key, val)
+    if "CPU part" in fields:
+        return "%s (implementer %s, part %s)" % (platform.machine(),
+                                                fields.get("CPU implementer", "?"),
+                                                fields["CPU part"])
+    return platform.machine()
+
+
 def oracle_seconds(wl, host, threads, a4w4=False):
     """Time the CPU oracle, as it stands, on the prepared token sample."""
     import oracle
@@ -215,7 +238,8 @@ def run_reference(args, wl):
         "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I,
                    "a4w4": bool(args.a4w4)},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": "first %d tokens of the workload per step, full layer" % n},
+                         "sample": "first %d tokens of the workload per step, full layer" % n,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -321,7 +345,8 @@ def run_step(args, wl):
         "roofline": roof, "gpu_launches": (len(bufs) + sum(splits)) * args.steps,
         "tflops": flops / (ms / 1e3) / 1e12,
         "cpu_baseline": {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d tokens, all GEMMs of the step (%.1f s)" % (n, dt)},
+                         "sample": "%d tokens, all GEMMs of the step (%.1f s)" % (n, dt),
+                         "cpu_model": cpu_model()},
         "clocks": sampler.summary(),
     }
     print(json.dumps(line))
@@ -561,7 +586,8 @@ def main():
         cores = os.cpu_count() or 1
         dt = oracle_seconds(wl, oracle_inputs(L, n), cores, a4w4=args.a4w4)
         cpu = {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": "first %d of %d tokens, full layer (%.1f s)" % (n, T, dt)}
+               "sample": "first %d of %d tokens, full layer (%.1f s)" % (n, T, dt),
+               "cpu_model": cpu_model()}
 
     if rank == 0:
         line = {
