@@ -2,8 +2,8 @@
 //
 // The layer ends with the weighted sum of the token's k expert outputs (the
 // routed-MoE layer of "Kimi K3.1 Pro at a glance"). One thread per 8 outputs
-// of a token: k 16-byte loads of grouped rows, fp32 fused multiply-adds in
-// j order, one 16-byte bf16 store. Every byte of y is written once, every
+// of a token: k 16-byte loads of grouped rows (issued 16 at a time), fp32
+// fused multiply-adds in j order, one 16-byte bf16 store. Every byte of y is written once, every
 // row of Yp is read once.
 #include "internal.h"
 
@@ -12,7 +12,12 @@ namespace moe {
 namespace {
 
 constexpr int kCombineThreads = 256;
+// Small batches (decode: one wave of threads, each waiting on its loads)
+// issue all 16 terms' loads together; large batches keep occupancy instead.
+constexpr int kSmallBatchThreads = 152 * 2048;
+constexpr int kLargeBatch = 4;
 
+template <int kBatch>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const uint4* __restrict__ yp, const int* __restrict__ slot_to_row,
                    const float* __restrict__ w, int k, int d, uint4* __restrict__ y,
@@ -25,15 +30,30 @@ __global__ void __launch_bounds__(kCombineThreads)
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const int64_t row = __ldg(slot_to_row + t * k + j);
-    const float wj = __ldg(w + t * k + j);
-    const uint4 q = __ldcs(yp + row * vpr + v);
-    const uint32_t q4[4] = {q.x, q.y, q.z, q.w};
+  // kBatch terms at a time: their row indices, then their row loads, are
+  // issued back to back (two memory latencies per batch, not two per term);
+  // the sums still run in j order.
+  for (int j0 = 0; j0 < k; j0 += kBatch) {
+    int row[kBatch];
+    float wj[kBatch];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] = fmaf(wj, __uint_as_float(q4[i] << 16), acc[2 * i]);
-      acc[2 * i + 1] = fmaf(wj, __uint_as_float(q4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+    for (int q = 0; q < kBatch; ++q) {
+      row[q] = j0 + q < k ? __ldg(slot_to_row + t * k + j0 + q) : 0;
+      wj[q] = j0 + q < k ? __ldg(w + t * k + j0 + q) : 0.0f;
+    }
+    uint4 val[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q)
+      val[q] = j0 + q < k ? __ldcs(yp + int64_t(row[q]) * vpr + v) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      if (j0 + q >= k) break;
+      const uint32_t q4[4] = {val[q].x, val[q].y, val[q].z, val[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(wj[q], __uint_as_float(q4[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wj[q], __uint_as_float(q4[i] & 0xFFFF0000u), acc[2 * i + 1]);
+      }
     }
   }
   uint32_t o[4];
@@ -52,9 +72,14 @@ cudaError_t launch_combine(const uint16_t* yp, const int* slot_to_row, const flo
   const int64_t total = int64_t(T) * (d / 8);
   if (total == 0) return cudaSuccess;
   const int64_t blocks = (total + kCombineThreads - 1) / kCombineThreads;
-  combine_kernel<<<dim3(unsigned(blocks)), kCombineThreads, 0, st>>>(
-      reinterpret_cast<const uint4*>(yp), slot_to_row, w, k, d, reinterpret_cast<uint4*>(y),
-      total);
+  if (total <= kSmallBatchThreads)
+    combine_kernel<16><<<dim3(unsigned(blocks)), kCombineThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(yp), slot_to_row, w, k, d, reinterpret_cast<uint4*>(y),
+        total);
+  else
+    combine_kernel<kLargeBatch><<<dim3(unsigned(blocks)), kCombineThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(yp), slot_to_row, w, k, d, reinterpret_cast<uint4*>(y),
+        total);
   return cudaGetLastError();
 }
 

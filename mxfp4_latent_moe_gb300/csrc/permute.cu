@@ -24,6 +24,16 @@ namespace {
 
 constexpr int kChunk = 256;  // tokens per block
 constexpr int kWarps = kChunk / 32;
+constexpr int kIdBatch = 16;  // expert ids of a token loaded together
+
+// Expert ids j0 .. j0 + 15 of token t (those below k): independent loads
+// issued back to back, so a token pays one memory latency per 16 ids.
+__device__ __forceinline__ void load_ids(const int* __restrict__ ids, int t, int k, int j0,
+                                         int (&idv)[kIdBatch]) {
+#pragma unroll
+  for (int q = 0; q < kIdBatch; ++q)
+    idv[q] = j0 + q < k ? __ldg(ids + int64_t(t) * k + j0 + q) : 0;
+}
 
 // Builds the per-warp expert masks of one chunk. An id out of range or
 // repeated within a token records MOE_ERR_DEVICE_BAD_INPUT and is skipped
@@ -35,14 +45,20 @@ __device__ __forceinline__ void build_masks(const int* __restrict__ ids, int T, 
   __syncthreads();
   const int t = blockIdx.x * kChunk + threadIdx.x;
   if (t < T) {
-    for (int j = 0; j < k; ++j) {
-      const int e = ids[int64_t(t) * k + j];
-      if (e < 0 || e >= E) {
-        set_status(status, MOE_ERR_DEVICE_BAD_INPUT);
-        continue;
+    for (int j0 = 0; j0 < k; j0 += kIdBatch) {
+      int idv[kIdBatch];
+      load_ids(ids, t, k, j0, idv);
+#pragma unroll
+      for (int q = 0; q < kIdBatch; ++q) {
+        if (j0 + q >= k) break;
+        const int e = idv[q];
+        if (e < 0 || e >= E) {
+          set_status(status, MOE_ERR_DEVICE_BAD_INPUT);
+          continue;
+        }
+        const uint32_t old = atomicOr(&masks[warp * E + e], 1u << lane);
+        if (old & (1u << lane)) set_status(status, MOE_ERR_DEVICE_BAD_INPUT);
       }
-      const uint32_t old = atomicOr(&masks[warp * E + e], 1u << lane);
-      if (old & (1u << lane)) set_status(status, MOE_ERR_DEVICE_BAD_INPUT);
     }
   }
   __syncthreads();
@@ -116,53 +132,59 @@ __global__ void __launch_bounds__(kChunk) permute_scatter_kernel(
   const int t = blockIdx.x * kChunk + threadIdx.x;
   if (t >= T) return;
   const uint32_t lower = (1u << lane) - 1u;
-  for (int j = 0; j < k; ++j) {
-    const int e = ids[int64_t(t) * k + j];
-    if (e < 0 || e >= E) continue;
-    int rank = __popc(masks[warp * E + e] & lower);
-    for (int w = 0; w < warp; ++w) rank += __popc(masks[w * E + e]);
-    const int row = offsets[e] + hist[int64_t(blockIdx.x) * E + e] + rank;
-    const int slot = t * k + j;
-    slot_to_row[slot] = row;
-    row_to_slot[row] = slot;
+  for (int j0 = 0; j0 < k; j0 += kIdBatch) {
+    int idv[kIdBatch];
+    load_ids(ids, t, k, j0, idv);
+#pragma unroll
+    for (int q = 0; q < kIdBatch; ++q) {
+      if (j0 + q >= k) break;
+      const int e = idv[q];
+      if (e < 0 || e >= E) continue;
+      int rank = __popc(masks[warp * E + e] & lower);
+      for (int w = 0; w < warp; ++w) rank += __popc(masks[w * E + e]);
+      const int row = offsets[e] + hist[int64_t(blockIdx.x) * E + e] + rank;
+      const int slot = t * k + j0 + q;
+      slot_to_row[slot] = row;
+      row_to_slot[row] = slot;
+    }
   }
 }
 
 // Batches of one chunk (T <= 256, decode): histogram, scan and scatter in
-// one block, row_to_slot filled with -1 first (one launch instead of three
-// and a memset). Same masks and ranks as the three kernels above.
-__global__ void __launch_bounds__(kChunk)
+// one block of 1024 threads, row_to_slot filled with -1 first (one launch
+// instead of three and a memset). Threads 0..255 own the tokens (same masks
+// and ranks as the three kernels above); all 1024 share the fill, the mask
+// clearing and the scan (one expert per thread, E <= 1024).
+constexpr int kSingleThreads = 1024;
+
+__global__ void __launch_bounds__(kSingleThreads)
     permute_single_kernel(const int* __restrict__ ids, int T, int E, int k, int pad_m,
                           int* __restrict__ counts, int* __restrict__ offsets,
                           int* __restrict__ slot_to_row, int* __restrict__ row_to_slot,
                           int64_t rows_capacity, int* status) {
   extern __shared__ uint32_t masks[];            // [kWarps][E], then offsets [E+1]
   int* off_s = reinterpret_cast<int*>(masks + kWarps * E);
-  __shared__ int warp_sums[kWarps];
+  __shared__ int warp_sums[kSingleThreads / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   {
     int64_t done = 0;
     if ((reinterpret_cast<uintptr_t>(row_to_slot) & 15u) == 0) {
       int4* r4 = reinterpret_cast<int4*>(row_to_slot);
-      for (int64_t i = tid; i < rows_capacity / 4; i += kChunk) r4[i] = make_int4(-1, -1, -1, -1);
+      for (int64_t i = tid; i < rows_capacity / 4; i += kSingleThreads)
+        r4[i] = make_int4(-1, -1, -1, -1);
       done = (rows_capacity / 4) * 4;
     }
-    for (int64_t i = done + tid; i < rows_capacity; i += kChunk) row_to_slot[i] = -1;
+    for (int64_t i = done + tid; i < rows_capacity; i += kSingleThreads) row_to_slot[i] = -1;
   }
   build_masks(ids, T, E, k, masks, status);      // ends with __syncthreads
-  // experts 4 tid .. 4 tid + 3: counts, padded sizes, block-wide exclusive scan
-  int cnt[4], pad[4], sum = 0;
+  // expert tid: count, padded size, block-wide exclusive scan
+  const int e = tid;
+  int cnt = 0;
+  if (e < E)
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int e = 4 * tid + q;
-    cnt[q] = 0;
-    if (e < E)
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) cnt[q] += __popc(masks[w * E + e]);
-    pad[q] = (cnt[q] + pad_m - 1) / pad_m * pad_m;
-    sum += pad[q];
-  }
-  int incl = sum;
+    for (int w = 0; w < kWarps; ++w) cnt += __popc(masks[w * E + e]);
+  const int padded = e < E ? (cnt + pad_m - 1) / pad_m * pad_m : 0;
+  int incl = padded;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int n = __shfl_up_sync(0xffffffffu, incl, off);
@@ -170,35 +192,46 @@ __global__ void __launch_bounds__(kChunk)
   }
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
-  int base = incl - sum;
-  for (int w = 0; w < warp; ++w) base += warp_sums[w];
+  if (warp == 0) {
+    const int s = warp_sums[lane];
+    int si = s;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int e = 4 * tid + q;
-    if (e < E) {
-      counts[e] = cnt[q];
-      offsets[e] = base;
-      off_s[e] = base;
-      if (e == E - 1) {
-        offsets[E] = base + pad[q];
-        off_s[E] = base + pad[q];
-      }
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, si, off);
+      if (lane >= off) si += n;
     }
-    base += pad[q];
+    warp_sums[lane] = si - s;  // exclusive over warps
+  }
+  __syncthreads();
+  if (e < E) {
+    const int base = incl - padded + warp_sums[warp];
+    counts[e] = cnt;
+    offsets[e] = base;
+    off_s[e] = base;
+    if (e == E - 1) {
+      offsets[E] = base + padded;
+      off_s[E] = base + padded;
+    }
   }
   __syncthreads();
   const int t = tid;
   if (t >= T) return;
   const uint32_t lower = (1u << lane) - 1u;
-  for (int j = 0; j < k; ++j) {
-    const int e = ids[int64_t(t) * k + j];
-    if (e < 0 || e >= E) continue;
-    int rank = __popc(masks[warp * E + e] & lower);
-    for (int w = 0; w < warp; ++w) rank += __popc(masks[w * E + e]);
-    const int row = off_s[e] + rank;
-    const int slot = t * k + j;
-    slot_to_row[slot] = row;
-    row_to_slot[row] = slot;
+  for (int j0 = 0; j0 < k; j0 += kIdBatch) {
+    int idv[kIdBatch];
+    load_ids(ids, t, k, j0, idv);
+#pragma unroll
+    for (int q = 0; q < kIdBatch; ++q) {
+      if (j0 + q >= k) break;
+      const int ex = idv[q];
+      if (ex < 0 || ex >= E) continue;
+      int rank = __popc(masks[warp * E + ex] & lower);
+      for (int w = 0; w < warp; ++w) rank += __popc(masks[w * E + ex]);
+      const int row = off_s[ex] + rank;
+      const int slot = t * k + j0 + q;
+      slot_to_row[slot] = row;
+      row_to_slot[row] = slot;
+    }
   }
 }
 
@@ -215,7 +248,7 @@ cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* 
   const int C = (T + kChunk - 1) / kChunk;
   const size_t smem = size_t(kWarps) * E * sizeof(uint32_t);
   if (C == 1 && row_to_slot) {   // one chunk: a single launch
-    permute_single_kernel<<<1, kChunk, smem + size_t(E + 1) * sizeof(int), st>>>(
+    permute_single_kernel<<<1, kSingleThreads, smem + size_t(E + 1) * sizeof(int), st>>>(
         ids, T, E, k, pad_m, counts, offsets, slot_to_row, row_to_slot, rows_capacity, status);
     return cudaGetLastError();
   }

@@ -20,6 +20,21 @@ namespace moe {
 namespace {
 
 constexpr int kQuantThreads = 256;
+// Grouped rows of a token looked up together: all 16 for small batches
+// (decode: one wave of threads, each waiting on its loads); one at a time for
+// large ones, which keep occupancy instead.
+constexpr int kSmallBatchThreads = 152 * 2048;
+constexpr int kLargeBatch = 1;
+
+// Grouped rows j0 .. j0 + B - 1 of token t (below nrows; the dense layout's
+// row is t): independent loads issued back to back.
+template <int B>
+__device__ __forceinline__ void load_rows(const int* __restrict__ slot_to_row, int64_t t, int k,
+                                          int nrows, int j0, int (&rows)[B]) {
+#pragma unroll
+  for (int q = 0; q < B; ++q)
+    rows[q] = j0 + q >= nrows ? 0 : slot_to_row ? __ldg(slot_to_row + t * k + j0 + q) : int(t);
+}
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -30,7 +45,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
   }
 }
 
-template <int LAYOUT>
+template <int LAYOUT, int kRowBatch>
 __global__ void __launch_bounds__(kQuantThreads)
     quant_mxfp8_kernel(const uint4* __restrict__ x, int d, const int* __restrict__ slot_to_row,
                        int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
@@ -63,13 +78,19 @@ __global__ void __launch_bounds__(kQuantThreads)
   const int64_t t = g / vpr;
   const int v = int(g - t * vpr);
   const int nrows = slot_to_row ? k : 1;
-  for (int j = 0; j < nrows; ++j) {
-    const int64_t row = slot_to_row ? int64_t(__ldg(slot_to_row + t * k + j)) : t;
-    *reinterpret_cast<uint2*>(codes + row * d + int64_t(v) * 8) = packed;
-    if ((lane & 15) == 0) {
-      const int64_t off = LAYOUT == kScalesGroup32 ? group32_sf_offset(row, int64_t(v >> 2), d)
-                                                   : tiled_sf_offset(row, int64_t(v >> 2), d);
-      *reinterpret_cast<uint32_t*>(scales + off) = sword;
+  for (int j0 = 0; j0 < nrows; j0 += kRowBatch) {
+    int rows[kRowBatch];
+    load_rows<kRowBatch>(slot_to_row, t, k, nrows, j0, rows);
+#pragma unroll
+    for (int q = 0; q < kRowBatch; ++q) {
+      if (j0 + q >= nrows) break;
+      const int64_t row = rows[q];
+      *reinterpret_cast<uint2*>(codes + row * d + int64_t(v) * 8) = packed;
+      if ((lane & 15) == 0) {
+        const int64_t off = LAYOUT == kScalesGroup32 ? group32_sf_offset(row, int64_t(v >> 2), d)
+                                                     : tiled_sf_offset(row, int64_t(v >> 2), d);
+        *reinterpret_cast<uint32_t*>(scales + off) = sword;
+      }
     }
   }
 }
@@ -78,7 +99,7 @@ __global__ void __launch_bounds__(kQuantThreads)
 // elements and shared exponent floor(log2(amax)) - 2; a thread's 8 codes are
 // one 32-bit word of the packed [rows][d/2] output (even element in the low
 // nibble of each byte).
-template <int LAYOUT>
+template <int LAYOUT, int kRowBatch>
 __global__ void __launch_bounds__(kQuantThreads)
     quant_mxfp4_kernel(const uint4* __restrict__ x, int d, const int* __restrict__ slot_to_row,
                        int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
@@ -110,13 +131,19 @@ __global__ void __launch_bounds__(kQuantThreads)
   const int64_t t = g / vpr;
   const int v = int(g - t * vpr);
   const int nrows = slot_to_row ? k : 1;
-  for (int j = 0; j < nrows; ++j) {
-    const int64_t row = slot_to_row ? int64_t(__ldg(slot_to_row + t * k + j)) : t;
-    *reinterpret_cast<uint32_t*>(codes + row * (d >> 1) + int64_t(v) * 4) = packed;
-    if ((lane & 15) == 0) {
-      const int64_t off = LAYOUT == kScalesGroup32 ? group32_sf_offset(row, int64_t(v >> 2), d)
-                                                   : tiled_sf_offset(row, int64_t(v >> 2), d);
-      *reinterpret_cast<uint32_t*>(scales + off) = sword;
+  for (int j0 = 0; j0 < nrows; j0 += kRowBatch) {
+    int rows[kRowBatch];
+    load_rows<kRowBatch>(slot_to_row, t, k, nrows, j0, rows);
+#pragma unroll
+    for (int q = 0; q < kRowBatch; ++q) {
+      if (j0 + q >= nrows) break;
+      const int64_t row = rows[q];
+      *reinterpret_cast<uint32_t*>(codes + row * (d >> 1) + int64_t(v) * 4) = packed;
+      if ((lane & 15) == 0) {
+        const int64_t off = LAYOUT == kScalesGroup32 ? group32_sf_offset(row, int64_t(v >> 2), d)
+                                                     : tiled_sf_offset(row, int64_t(v >> 2), d);
+        *reinterpret_cast<uint32_t*>(scales + off) = sword;
+      }
     }
   }
 }
@@ -160,12 +187,24 @@ cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_
   const int64_t total = int64_t(T) * (d / 8);
   if (total == 0 || (slot_to_row && k == 0)) return cudaSuccess;
   const int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
-  if (layout == kScalesGroup32)
-    quant_mxfp8_kernel<kScalesGroup32><<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
-  else
-    quant_mxfp8_kernel<kScalesTiled128><<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
+  const dim3 grid(static_cast<unsigned>(blocks));
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  const bool small = total <= kSmallBatchThreads;
+  if (layout == kScalesGroup32) {
+    if (small)
+      quant_mxfp8_kernel<kScalesGroup32, 16><<<grid, kQuantThreads, 0, st>>>(xv, d, slot_to_row, k,
+                                                                          codes, scales, total);
+    else
+      quant_mxfp8_kernel<kScalesGroup32, kLargeBatch><<<grid, kQuantThreads, 0, st>>>(
+          xv, d, slot_to_row, k, codes, scales, total);
+  } else {
+    if (small)
+      quant_mxfp8_kernel<kScalesTiled128, 16><<<grid, kQuantThreads, 0, st>>>(xv, d, slot_to_row, k,
+                                                                           codes, scales, total);
+    else
+      quant_mxfp8_kernel<kScalesTiled128, kLargeBatch><<<grid, kQuantThreads, 0, st>>>(
+          xv, d, slot_to_row, k, codes, scales, total);
+  }
   return cudaGetLastError();
 }
 
@@ -174,12 +213,24 @@ cudaError_t launch_quant_mxfp4(const uint16_t* x, int T, int d, const int* slot_
   const int64_t total = int64_t(T) * (d / 8);
   if (total == 0 || (slot_to_row && k == 0)) return cudaSuccess;
   const int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
-  if (layout == kScalesGroup32)
-    quant_mxfp4_kernel<kScalesGroup32><<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
-  else
-    quant_mxfp4_kernel<kScalesTiled128><<<dim3(unsigned(blocks)), kQuantThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(x), d, slot_to_row, k, codes, scales, total);
+  const dim3 grid(static_cast<unsigned>(blocks));
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  const bool small = total <= kSmallBatchThreads;
+  if (layout == kScalesGroup32) {
+    if (small)
+      quant_mxfp4_kernel<kScalesGroup32, 16><<<grid, kQuantThreads, 0, st>>>(xv, d, slot_to_row, k,
+                                                                          codes, scales, total);
+    else
+      quant_mxfp4_kernel<kScalesGroup32, kLargeBatch><<<grid, kQuantThreads, 0, st>>>(
+          xv, d, slot_to_row, k, codes, scales, total);
+  } else {
+    if (small)
+      quant_mxfp4_kernel<kScalesTiled128, 16><<<grid, kQuantThreads, 0, st>>>(xv, d, slot_to_row, k,
+                                                                           codes, scales, total);
+    else
+      quant_mxfp4_kernel<kScalesTiled128, kLargeBatch><<<grid, kQuantThreads, 0, st>>>(
+          xv, d, slot_to_row, k, codes, scales, total);
+  }
   return cudaGetLastError();
 }
 

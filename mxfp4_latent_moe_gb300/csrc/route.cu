@@ -6,9 +6,12 @@
 // weights are sigmoid(l_j) / sum of the k selected sigmoids.
 //
 // Each lane holds the logits of experts lane, lane+32, ... (up to 32 per lane
-// for E <= 1024) in registers and keeps its two best untaken ones. k rounds
-// of a warp-wide (value desc, id asc) arg-max of the lanes' heads by
-// butterfly shuffles pick the experts in output order. Reads are coalesced: a
+// for E <= 1024) as 64-bit keys that order like (value desc, id asc): the
+// high word maps the float monotonically onto unsigned integers (-0 joins +0),
+// the low word is ~id. A lane keeps its two best untaken keys (branch-free
+// max/min updates); each of the k rounds takes the warp's best head with two
+// warp reductions (max of the high words, then max of the low words among the
+// lanes that hold it), and the owning lane pops it. Reads are coalesced: a
 // token's row is read once.
 #include "internal.h"
 
@@ -18,32 +21,32 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
+// Monotone map of a float onto uint32 (a < b <=> key(a) < key(b); -0 and +0
+// share a key) and its inverse (which returns +0 for both zeros).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// (value, id) -> 64-bit key; larger is better. 0 is below every real key.
+__device__ __forceinline__ uint64_t route_key(float v, int e) {
+  return (uint64_t(order_key(v)) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(e));
 }
 
-// The lane's best two values (by `better`) among those worse than (lv, li)
-// when `limit`, else among all of its values; sentinels (-inf, INT_MAX) fill.
+// The lane's best two keys (a > b) among those below `limit` (all when limit
+// is ~0); 0 fills a missing one.
 template <int NPL>
-__device__ __forceinline__ void lane_top2(const float (&v)[NPL], int E, int lane, bool limit,
-                                          float lv, int li, float& av, int& ai, float& bv,
-                                          int& bi) {
-  av = bv = -INFINITY;
-  ai = bi = 0x7FFFFFFF;
+__device__ __forceinline__ void lane_top2(const uint64_t (&key)[NPL], uint64_t limit, uint64_t& a,
+                                          uint64_t& b) {
+  a = b = 0;
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E && (!limit || better(lv, li, v[i], e)) && better(v[i], e, bv, bi)) {
-      if (better(v[i], e, av, ai)) {
-        bv = av;
-        bi = ai;
-        av = v[i];
-        ai = e;
-      } else {
-        bv = v[i];
-        bi = e;
-      }
-    }
+    const uint64_t x = key[i] < limit ? key[i] : 0;
+    const uint64_t lo = a < x ? a : x;
+    a = a < x ? x : a;
+    b = b < lo ? lo : b;
   }
 }
 
@@ -55,54 +58,40 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;  // warp-uniform
   const float* row = logits + int64_t(t) * E;
-  float v[NPL];
+  uint64_t key[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? __ldg(row + e) : -INFINITY;
+    key[i] = e < E ? route_key(__ldg(row + e), e) : 0;
   }
-  // Each lane keeps its two best untaken values; a round is a warp arg-max of
-  // the lanes' heads (value desc, id asc) and a pop on the winning lane. The
-  // values a lane has given up are always its best ones, so once its two are
-  // gone it rescans for the best two below its last pick.
-  float av, bv;
-  int ai, bi;
-  lane_top2<NPL>(v, E, lane, false, 0.0f, 0, av, ai, bv, bi);
-  float my_v = 0.0f;
-  int my_id = 0;
+  // A lane gives up its keys in descending order, so once its two are taken
+  // it rescans for the best two below the last one it gave up.
+  uint64_t a, b;
+  lane_top2<NPL>(key, ~uint64_t(0), a, b);
+  uint32_t my_hi = 0, my_lo = 0;
   for (int j = 0; j < k; ++j) {
-    float wv = av;
-    int wi = ai;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, wv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, wi, off);
-      if (better(ov, oi, wv, wi)) {
-        wv = ov;
-        wi = oi;
-      }
-    }
-    if ((wi & 31) == lane) {   // this lane's head won: pop it
-      const float lv = av;
-      const int li = ai;
-      av = bv;
-      ai = bi;
-      bv = -INFINITY;
-      bi = 0x7FFFFFFF;
-      if (ai == 0x7FFFFFFF) lane_top2<NPL>(v, E, lane, true, lv, li, av, ai, bv, bi);
+    const uint32_t hi = uint32_t(a >> 32), lo = uint32_t(a);
+    const uint32_t m_hi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t m_lo = __reduce_max_sync(0xffffffffu, hi == m_hi ? lo : 0u);
+    const int id = int(0xFFFFFFFFu - m_lo);
+    if ((id & 31) == lane) {   // this lane's head won: pop it
+      const uint64_t taken = a;
+      a = b;
+      b = 0;
+      if (a == 0) lane_top2<NPL>(key, taken, a, b);
     }
     if (lane == j) {
-      my_v = wv;
-      my_id = wi;
+      my_hi = m_hi;
+      my_lo = m_lo;
     }
   }
   // sigmoid of the selected logits, renormalised over the k of them
-  const float s = lane < k ? 1.0f / (1.0f + expf(-my_v)) : 0.0f;
+  const float s = lane < k ? 1.0f / (1.0f + expf(-key_value(my_hi))) : 0.0f;
   float sum = s;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
   if (lane < k) {
-    ids[int64_t(t) * k + lane] = my_id;
+    ids[int64_t(t) * k + lane] = int(0xFFFFFFFFu - my_lo);
     w[int64_t(t) * k + lane] = s / sum;
   }
 }
