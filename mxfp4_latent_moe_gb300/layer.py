@@ -79,3 +79,67 @@ class MoeLayer:
         with torch.cuda.graph(g):
             self.forward(x, logits, ws=ws, y=y, topk_ids=topk_ids, topk_w=topk_w, a4w4=a4w4)
         return g, y, ws
+
+
+class HostPipeline:
+    """Runs the layer on batches held in (pinned) host memory with the copies
+    off the compute stream.
+
+    Batch i's inputs go host -> device on a copy stream while batch i-1
+    computes; its output goes device -> host on a second copy stream while
+    batch i+1 computes. `depth` sets of device buffers rotate; a set is
+    refilled only after the forward that read it has finished, and its y only
+    after the copy that drained it. submit() enqueues and returns at once;
+    y_h holds batch i's result once synchronize() (or the event submit
+    returns) has completed. All batches have T tokens.
+    """
+
+    def __init__(self, layer, T, depth=2, a4w4=False, device=None):
+        dev = device or layer.w13.device
+        self.layer, self.T, self.a4w4 = layer, T, a4w4
+        self.compute = torch.cuda.current_stream(dev)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.ws = layer.workspace(T)
+        self.sets = []
+        for _ in range(depth):
+            self.sets.append({
+                "x": torch.empty(T, layer.d, dtype=torch.bfloat16, device=dev),
+                "logits": torch.empty(T, layer.E, dtype=torch.float32, device=dev),
+                "y": torch.empty(T, layer.d, dtype=torch.bfloat16, device=dev),
+                "in_ready": torch.cuda.Event(), "inputs_free": None, "y_free": None,
+            })
+        self.n = 0
+
+    def submit(self, x_h, logits_h, y_h):
+        """Enqueues one batch: x_h bf16 [T][d], logits_h fp32 [T][E] in,
+        y_h bf16 [T][d] out (host tensors, pinned for asynchronous copies).
+        Returns an event that completes when y_h holds the result."""
+        b = self.sets[self.n % len(self.sets)]
+        self.n += 1
+        with torch.cuda.stream(self.h2d):
+            if b["inputs_free"] is not None:
+                self.h2d.wait_event(b["inputs_free"])
+            b["x"].copy_(x_h, non_blocking=True)
+            b["logits"].copy_(logits_h, non_blocking=True)
+            b["in_ready"].record(self.h2d)
+        self.compute.wait_event(b["in_ready"])
+        if b["y_free"] is not None:
+            self.compute.wait_event(b["y_free"])
+        self.layer.forward(b["x"], b["logits"], ws=self.ws, y=b["y"], stream=self.compute,
+                           a4w4=self.a4w4)
+        done = torch.cuda.Event()
+        done.record(self.compute)
+        b["inputs_free"] = done
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(done)
+            y_h.copy_(b["y"], non_blocking=True)
+            out = torch.cuda.Event()
+            out.record(self.d2h)
+        b["y_free"] = out
+        return out
+
+    def synchronize(self):
+        self.h2d.synchronize()
+        self.compute.synchronize()
+        self.d2h.synchronize()

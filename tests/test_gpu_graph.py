@@ -46,3 +46,24 @@ def test_graph_replay_matches_eager(abi, wl, kernel, a4w4):
         torch.cuda.synchronize()
         assert torch.equal(got_ids, ref_ids)
         assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), step
+
+
+def test_host_pipeline_matches_forward(abi):
+    """Batches through HostPipeline (copies on their own streams, two device
+    buffer sets rotating) give bit-identical outputs to eager forwards, in
+    order, for more batches than buffer sets."""
+    from mxfp4_latent_moe_gb300.layer import HostPipeline
+    wl = synth.shape("pipe", T=24, d=256, E=16, k=4, I=256)
+    L = synth.make_layer(wl, seed=5, device="cuda")
+    layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k)
+    n = 5
+    xs = [synth.make_activations(wl, seed=100 + i) for i in range(n)]
+    want = [layer.forward(x.cuda(), lg.cuda()).cpu() for x, lg in xs]
+    pipe = HostPipeline(layer, wl.T)
+    outs = [torch.empty(wl.T, wl.d, dtype=torch.bfloat16).pin_memory() for _ in range(n)]
+    for (x, lg), y_h in zip(xs, outs):
+        pipe.submit(x.pin_memory(), lg.pin_memory(), y_h)
+    pipe.synchronize()
+    assert abi.moe_check_device_status(pipe.ws) == 0
+    for got, ref in zip(outs, want):
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
