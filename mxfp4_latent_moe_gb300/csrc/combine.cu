@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const uint4* __restrict__ yp, const int* __restrict__ slot_to_row,
                    const float* __restrict__ w, int k, int d, uint4* __restrict__ y,
                    int64_t total_vec) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t g = int64_t(blockIdx.x) * kCombineThreads + threadIdx.x;
   if (g >= total_vec) return;
   const int vpr = d >> 3;
@@ -72,15 +74,14 @@ cudaError_t launch_combine(const uint16_t* yp, const int* slot_to_row, const flo
   const int64_t total = int64_t(T) * (d / 8);
   if (total == 0) return cudaSuccess;
   const int64_t blocks = (total + kCombineThreads - 1) / kCombineThreads;
-  if (total <= kSmallBatchThreads)
-    combine_kernel<16><<<dim3(unsigned(blocks)), kCombineThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(yp), slot_to_row, w, k, d, reinterpret_cast<uint4*>(y),
-        total);
-  else
-    combine_kernel<kLargeBatch><<<dim3(unsigned(blocks)), kCombineThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(yp), slot_to_row, w, k, d, reinterpret_cast<uint4*>(y),
-        total);
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(blocks));
+  const uint4* ypv = reinterpret_cast<const uint4*>(yp);
+  uint4* yv = reinterpret_cast<uint4*>(y);
+  if (total <= kSmallBatchThreads)   // decode-sized
+    return launch_ex(true, combine_kernel<16>, grid, dim3(kCombineThreads), 0, st, 1, ypv,
+                     slot_to_row, w, k, d, yv, total);
+  return launch_ex(false, combine_kernel<kLargeBatch>, grid, dim3(kCombineThreads), 0, st, 1, ypv,
+                   slot_to_row, w, k, d, yv, total);
 }
 
 }  // namespace moe

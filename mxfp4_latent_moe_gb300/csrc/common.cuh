@@ -21,6 +21,53 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch. The layer's latency-bound kernels are
+// launched with programmatic stream serialisation (launch_ex): a kernel may
+// start while the previous one in the stream is still running. Each kernel lets its successor launch
+// as soon as it starts (pdl_trigger), and waits for its predecessor to finish
+// and its writes to be visible (pdl_wait) before it touches memory that a
+// predecessor may write or read; only set-up (barriers, tensor memory,
+// shared memory) runs before the wait. Both are no-ops for a kernel launched
+// without the attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch, with programmatic stream serialisation when `pdl` (the layer's
+// latency-bound launches: the GEMMs and the decode-sized small kernels; the
+// prefill-sized small kernels measured slightly faster without it) and a
+// cluster of cluster_x CTAs along x when cluster_x > 1.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                             size_t smem, cudaStream_t st, int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = unsigned(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args...);
+  return err != cudaSuccess ? err : cudaGetLastError();
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

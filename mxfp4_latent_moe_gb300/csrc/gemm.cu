@@ -195,6 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
+  pdl_trigger();
+  pdl_wait();   // the groups and activations come from the previous kernels
   for (int i = threadIdx.x; i <= E; i += kThreads) {
     offs[i] = p.offsets[i];
     if (i < E) cnts[i] = p.counts[i];
@@ -584,17 +586,17 @@ cudaError_t launch_mode(const GemmParams& p, const CUtensorMap& ta, const CUtens
   const int64_t max_units = (p.rows_capacity / BM) * ((p.n_tiles + CL - 1) / CL);
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = st;
   int slots = sms;   // resident CTA groups: one CTA per SM
   if (CL > 1) {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(CL * sms);
@@ -603,15 +605,10 @@ cudaError_t launch_mode(const GemmParams& p, const CUtensorMap& ta, const CUtens
     if (err != cudaSuccess) return err;
     if (clusters <= 0) return cudaErrorInvalidConfiguration;
     slots = clusters;
-  } else {
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
   }
   const int64_t groups = max_units < slots ? (max_units > 0 ? max_units : 1) : slots;
-  cfg.gridDim = dim3(unsigned(groups * CL));
-  err = cudaLaunchKernelEx(&cfg, kernel, ta, tb, p);
-  if (err != cudaSuccess) return err;
-  return cudaGetLastError();
+  return launch_ex(true, kernel, dim3(unsigned(groups * CL)), dim3(kThreads), kSmemBytes, st, CL, ta,
+                    tb, p);
 }
 
 }  // namespace

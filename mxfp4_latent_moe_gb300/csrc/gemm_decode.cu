@@ -139,6 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
+  pdl_trigger();
+  pdl_wait();   // the groups and activations come from the previous kernels
   for (int i = threadIdx.x; i <= E; i += kThreads) {
     offs[i] = p.offsets[i];
     if (i < E) cnts[i] = p.counts[i];
@@ -375,8 +377,8 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tw, const CU
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int64_t max_tiles = (p.rows_capacity / NTOK) * p.n_tiles;
   const int grid = int(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
-  grouped_gemm_decode_kernel<MODE><<<grid, kThreads, kSmemBytes, st>>>(tw, tx, p);
-  return cudaGetLastError();
+  return launch_ex(true, grouped_gemm_decode_kernel<MODE>, dim3(grid), dim3(kThreads), kSmemBytes, st,
+                    1, tw, tx, p);
 }
 
 }  // namespace

@@ -42,6 +42,7 @@ __device__ __forceinline__ void build_masks(const int* __restrict__ ids, int T, 
                                            uint32_t* masks, int* status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) masks[i] = 0u;
+  pdl_wait();   // the ids come from the previous kernel
   __syncthreads();
   const int t = blockIdx.x * kChunk + threadIdx.x;
   if (t < T) {
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(kChunk) permute_count_kernel(const int* __rest
                                                                int* __restrict__ hist,
                                                                int* status) {
   extern __shared__ uint32_t masks[];
+  pdl_trigger();
   build_masks(ids, T, E, k, masks, status);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int s = 0;
@@ -83,6 +85,8 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int* __restrict__ hi
                                                             int pad_m, int* __restrict__ counts,
                                                             int* __restrict__ offsets) {
   __shared__ int warp_sums[32];
+  pdl_trigger();
+  pdl_wait();
   const int e = threadIdx.x;
   int cnt = 0;
   if (e < E) {
@@ -127,6 +131,7 @@ __global__ void __launch_bounds__(kChunk) permute_scatter_kernel(
     const int* __restrict__ offsets, int* __restrict__ slot_to_row, int* __restrict__ row_to_slot,
     int* status) {
   extern __shared__ uint32_t masks[];
+  pdl_trigger();
   build_masks(ids, T, E, k, masks, status);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kChunk + threadIdx.x;
@@ -166,7 +171,8 @@ __global__ void __launch_bounds__(kSingleThreads)
   int* off_s = reinterpret_cast<int*>(masks + kWarps * E);
   __shared__ int warp_sums[kSingleThreads / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  {
+  pdl_trigger();
+  {   // row_to_slot is written by no kernel before this one: filled before the wait
     int64_t done = 0;
     if ((reinterpret_cast<uintptr_t>(row_to_slot) & 15u) == 0) {
       int4* r4 = reinterpret_cast<int4*>(row_to_slot);
@@ -248,17 +254,17 @@ cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* 
   const int C = (T + kChunk - 1) / kChunk;
   const size_t smem = size_t(kWarps) * E * sizeof(uint32_t);
   if (C == 1 && row_to_slot) {   // one chunk: a single launch
-    permute_single_kernel<<<1, kSingleThreads, smem + size_t(E + 1) * sizeof(int), st>>>(
-        ids, T, E, k, pad_m, counts, offsets, slot_to_row, row_to_slot, rows_capacity, status);
-    return cudaGetLastError();
+    return launch_ex(true, permute_single_kernel, dim3(1), dim3(kSingleThreads),
+                      smem + size_t(E + 1) * sizeof(int), st, 1, ids, T, E, k, pad_m, counts,
+                      offsets, slot_to_row, row_to_slot, rows_capacity, status);
   }
   if (C > 0 && k > 0) {
-    permute_count_kernel<<<C, kChunk, smem, st>>>(ids, T, E, k, hist, status);
-    cudaError_t err = cudaGetLastError();
+    const cudaError_t err = launch_ex(false, permute_count_kernel, dim3(C), dim3(kChunk), smem,
+                                      st, 1, ids, T, E, k, hist, status);
     if (err != cudaSuccess) return err;
   }
-  permute_scan_kernel<<<1, 1024, 0, st>>>(hist, (k > 0) ? C : 0, E, pad_m, counts, offsets);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_ex(false, permute_scan_kernel, dim3(1), dim3(1024), 0, st, 1, hist,
+                              (k > 0) ? C : 0, E, pad_m, counts, offsets);
   if (err != cudaSuccess) return err;
   if (rows_capacity > 0 && row_to_slot) {
     err = cudaMemsetAsync(row_to_slot, 0xFF, size_t(rows_capacity) * sizeof(int), st);

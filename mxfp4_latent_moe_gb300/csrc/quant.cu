@@ -50,6 +50,8 @@ __global__ void __launch_bounds__(kQuantThreads)
     quant_mxfp8_kernel(const uint4* __restrict__ x, int d, const int* __restrict__ slot_to_row,
                        int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                        int64_t total_vec) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t g = int64_t(blockIdx.x) * kQuantThreads + threadIdx.x;
   const int lane = threadIdx.x & 31;
   const bool valid = g < total_vec;
@@ -104,6 +106,8 @@ __global__ void __launch_bounds__(kQuantThreads)
     quant_mxfp4_kernel(const uint4* __restrict__ x, int d, const int* __restrict__ slot_to_row,
                        int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                        int64_t total_vec) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t g = int64_t(blockIdx.x) * kQuantThreads + threadIdx.x;
   const int lane = threadIdx.x & 31;
   const bool valid = g < total_vec;
@@ -182,56 +186,50 @@ __global__ void prepack_weights_kernel(const uint4* __restrict__ src, int K,
 
 }  // namespace
 
-cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
-                               uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st) {
+namespace {
+
+template <int LAYOUT, int B>
+cudaError_t launch_quant_kernel(bool fp4, dim3 grid, cudaStream_t st, const uint4* x, int d,
+                                const int* slot_to_row, int k, uint8_t* codes, uint8_t* scales,
+                                int64_t total) {
+  const bool pdl = B == 16;   // decode-sized
+  if (fp4)
+    return launch_ex(pdl, quant_mxfp4_kernel<LAYOUT, B>, grid, dim3(kQuantThreads), 0, st, 1, x,
+                     d, slot_to_row, k, codes, scales, total);
+  return launch_ex(pdl, quant_mxfp8_kernel<LAYOUT, B>, grid, dim3(kQuantThreads), 0, st, 1, x, d,
+                   slot_to_row, k, codes, scales, total);
+}
+
+cudaError_t launch_quant(bool fp4, const uint16_t* x, int T, int d, const int* slot_to_row, int k,
+                         uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st) {
   const int64_t total = int64_t(T) * (d / 8);
   if (total == 0 || (slot_to_row && k == 0)) return cudaSuccess;
-  const int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
-  const dim3 grid(static_cast<unsigned>(blocks));
+  const dim3 grid(static_cast<unsigned>((total + kQuantThreads - 1) / kQuantThreads));
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const bool small = total <= kSmallBatchThreads;
-  if (layout == kScalesGroup32) {
-    if (small)
-      quant_mxfp8_kernel<kScalesGroup32, 16><<<grid, kQuantThreads, 0, st>>>(xv, d, slot_to_row, k,
-                                                                          codes, scales, total);
-    else
-      quant_mxfp8_kernel<kScalesGroup32, kLargeBatch><<<grid, kQuantThreads, 0, st>>>(
-          xv, d, slot_to_row, k, codes, scales, total);
-  } else {
-    if (small)
-      quant_mxfp8_kernel<kScalesTiled128, 16><<<grid, kQuantThreads, 0, st>>>(xv, d, slot_to_row, k,
-                                                                           codes, scales, total);
-    else
-      quant_mxfp8_kernel<kScalesTiled128, kLargeBatch><<<grid, kQuantThreads, 0, st>>>(
-          xv, d, slot_to_row, k, codes, scales, total);
-  }
-  return cudaGetLastError();
+  if (layout == kScalesGroup32)
+    return small ? launch_quant_kernel<kScalesGroup32, 16>(fp4, grid, st, xv, d, slot_to_row, k,
+                                                           codes, scales, total)
+                 : launch_quant_kernel<kScalesGroup32, kLargeBatch>(fp4, grid, st, xv, d,
+                                                                    slot_to_row, k, codes,
+                                                                    scales, total);
+  return small ? launch_quant_kernel<kScalesTiled128, 16>(fp4, grid, st, xv, d, slot_to_row, k,
+                                                          codes, scales, total)
+               : launch_quant_kernel<kScalesTiled128, kLargeBatch>(fp4, grid, st, xv, d,
+                                                                   slot_to_row, k, codes, scales,
+                                                                   total);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_mxfp8(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
+                               uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st) {
+  return launch_quant(false, x, T, d, slot_to_row, k, codes, scales, layout, st);
 }
 
 cudaError_t launch_quant_mxfp4(const uint16_t* x, int T, int d, const int* slot_to_row, int k,
                                uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st) {
-  const int64_t total = int64_t(T) * (d / 8);
-  if (total == 0 || (slot_to_row && k == 0)) return cudaSuccess;
-  const int64_t blocks = (total + kQuantThreads - 1) / kQuantThreads;
-  const dim3 grid(static_cast<unsigned>(blocks));
-  const uint4* xv = reinterpret_cast<const uint4*>(x);
-  const bool small = total <= kSmallBatchThreads;
-  if (layout == kScalesGroup32) {
-    if (small)
-      quant_mxfp4_kernel<kScalesGroup32, 16><<<grid, kQuantThreads, 0, st>>>(xv, d, slot_to_row, k,
-                                                                          codes, scales, total);
-    else
-      quant_mxfp4_kernel<kScalesGroup32, kLargeBatch><<<grid, kQuantThreads, 0, st>>>(
-          xv, d, slot_to_row, k, codes, scales, total);
-  } else {
-    if (small)
-      quant_mxfp4_kernel<kScalesTiled128, 16><<<grid, kQuantThreads, 0, st>>>(xv, d, slot_to_row, k,
-                                                                           codes, scales, total);
-    else
-      quant_mxfp4_kernel<kScalesTiled128, kLargeBatch><<<grid, kQuantThreads, 0, st>>>(
-          xv, d, slot_to_row, k, codes, scales, total);
-  }
-  return cudaGetLastError();
+  return launch_quant(true, x, T, d, slot_to_row, k, codes, scales, layout, st);
 }
 
 cudaError_t launch_prepack_scales(const uint8_t* src, int64_t rows, int K, uint8_t* dst,

@@ -54,6 +54,7 @@ template <int NPL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                       int* __restrict__ ids, float* __restrict__ w) {
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;  // warp-uniform
