@@ -446,7 +446,10 @@ def main():
     sampler.mark()
     total_ms = replicas.max_over_ranks(total_ms, dev)
     replicas.barrier()
-    launches_per_step = 8
+    # this library's kernels per forward: route, grouping (one kernel for a
+    # one-chunk batch of T <= 256 tokens, else count + scan + scatter),
+    # quantisation, the two GEMMs, combine
+    launches_per_step = 6 if T <= 256 else 8
 
     # ---- per-kernel breakdown: the same kernels through the step entry points
     rc = rows_cap
