@@ -115,6 +115,12 @@ class HostPipeline:
         """Enqueues one batch: x_h bf16 [T][d], logits_h fp32 [T][E] in,
         y_h bf16 [T][d] out (host tensors, pinned for asynchronous copies).
         Returns an event that completes when y_h holds the result."""
+        T, d, E = self.T, self.layer.d, self.layer.E
+        if (tuple(x_h.shape) != (T, d) or x_h.dtype != torch.bfloat16
+                or tuple(logits_h.shape) != (T, E) or logits_h.dtype != torch.float32
+                or tuple(y_h.shape) != (T, d) or y_h.dtype != torch.bfloat16):
+            raise ValueError("HostPipeline.submit: expected x bf16 [%d][%d], logits fp32 "
+                             "[%d][%d], y bf16 [%d][%d]" % (T, d, T, E, T, d))
         b = self.sets[self.n % len(self.sets)]
         self.n += 1
         with torch.cuda.stream(self.h2d):
