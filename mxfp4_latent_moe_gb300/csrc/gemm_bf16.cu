@@ -23,7 +23,9 @@
 // Calls with too few tiles to cover the GPU (decode: one row tile) split K:
 // each CTA accumulates one K-slice of a tile and writes its fp32 partial sums
 // to the workspace; a second kernel adds the slices in a fixed order and
-// applies the epilogue, so results do not depend on the split.
+// applies the epilogue, so results do not depend on the split. Both kernels
+// use programmatic dependent launch, so the reduction's launch and the next
+// GEMM's set-up overlap the running kernel.
 // Every wait is bounded (MOE_ERR_DEVICE_TIMEOUT in the status word).
 #include "internal.h"
 
@@ -130,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
+  pdl_trigger();
+  pdl_wait();   // the operands (and the partial-sum buffer) belong to earlier kernels
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -345,6 +349,8 @@ template <int EPI>
 __global__ void __launch_bounds__(256)
     bf16_splitk_reduce_kernel(const float* __restrict__ partial, int KS, int64_t M, int N,
                               void* __restrict__ c) {
+  pdl_trigger();
+  pdl_wait();
   const int n_out = EPI == kEpiSwiglu ? (N >> 1) : N;
   const int64_t g = int64_t(blockIdx.x) * 256 + threadIdx.x;   // group of 4 outputs
   const int64_t per_row = n_out >> 2;
@@ -402,9 +408,9 @@ cudaError_t launch_epi(const Bf16Params& p, const CUtensorMap& ta, const CUtenso
     if (err != cudaSuccess) return err;
     const int n_out = EPI == kEpiSwiglu ? (p.N >> 1) : p.N;
     const int64_t groups = p.M * (n_out / 4);
-    bf16_splitk_reduce_kernel<EPI><<<dim3(unsigned((groups + 255) / 256)), 256, 0, st>>>(
-        p.partial, p.KS, p.M, p.N, p.c);
-    return cudaGetLastError();
+    return launch_ex(true, bf16_splitk_reduce_kernel<EPI>, dim3(unsigned((groups + 255) / 256)),
+                     dim3(256), 0, st, 1, static_cast<const float*>(p.partial), p.KS, p.M, p.N,
+                     p.c);
   }
   return launch_epi_main<EPI>(p, ta, tb, st);
 }
@@ -420,8 +426,8 @@ cudaError_t launch_epi_main(const Bf16Params& p, const CUtensorMap& ta, const CU
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int64_t work = int64_t(p.MT) * p.NT * p.KS;
   const int grid = int(work < sms ? work : sms);
-  gemm_bf16_kernel<EPI><<<grid, kThreads, kSmemBytes, st>>>(ta, tb, p);
-  return cudaGetLastError();
+  return launch_ex(true, gemm_bf16_kernel<EPI>, dim3(grid), dim3(kThreads), kSmemBytes, st, 1, ta,
+                   tb, p);
 }
 
 }  // namespace
