@@ -23,6 +23,10 @@
  *    library never allocates or frees device memory and never synchronises,
  *    except moe_check_device_status.
  *  - Work is enqueued on `stream` in order; the host returns without waiting.
+ *    Most kernels use programmatic dependent launch: one may start while the
+ *    previous kernel in the stream is still running, but it reads and writes
+ *    no global memory until that kernel has finished (griddepcontrol.wait),
+ *    so stream order holds for the caller's kernels and copies as well.
  *  - Arguments are validated on the host before any launch. A failed check
  *    returns a non-zero moe_status and enqueues nothing.
  *  - Launch failures return MOE_ERR_CUDA. Problems found on the device (a
