@@ -24,9 +24,10 @@
  *    except moe_check_device_status.
  *  - Work is enqueued on `stream` in order; the host returns without waiting.
  *    Most kernels use programmatic dependent launch: one may start while the
- *    previous kernel in the stream is still running, but it reads and writes
- *    no global memory until that kernel has finished (griddepcontrol.wait),
- *    so stream order holds for the caller's kernels and copies as well.
+ *    previous kernel of this library in the stream is still running (after
+ *    any other kernel it starts only once that one has finished), and it
+ *    waits for its predecessor (griddepcontrol.wait) before touching memory
+ *    that kernel or the caller may use, so stream order holds as usual.
  *  - Arguments are validated on the host before any launch. A failed check
  *    returns a non-zero moe_status and enqueues nothing.
  *  - Launch failures return MOE_ERR_CUDA. Problems found on the device (a
