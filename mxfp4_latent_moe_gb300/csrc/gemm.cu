@@ -96,7 +96,20 @@ struct GemmParams {
   uint8_t* out_sf;       // MODE 0: hs TILED (rows, I)
   uint16_t* out_bf16;    // MODE 1: yp [rows][d]
   int* status;
+  bool out32;            // the output base is 32-byte aligned: 32-byte stores
 };
+
+// One 32-byte store (the address 32-byte aligned). A warp's 32 rows then
+// write whole 32-byte sectors; with 16-byte stores, which leave each sector
+// half written per request, the epilogue's stores cost the stage-2 kernel
+// about 1.7 times as much time.
+__device__ __forceinline__ void st_global_32B(void* dst, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                              uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0),
+               "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
 
 // ---- 2-CTA clusters: the A tile multicast to both CTAs of a pair ----------
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -517,8 +530,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (live) {
             uint4* dst = reinterpret_cast<uint4*>(p.out_q + row * p.I + int64_t(nt) * 128 +
                                                   (2 * half + c) * 32);
-            dst[0] = o[0];
-            dst[1] = o[1];
+            if (p.out32) {
+              st_global_32B(dst, o[0].x, o[0].y, o[0].z, o[0].w, o[1].x, o[1].y, o[1].z, o[1].w);
+            } else {
+              dst[0] = o[0];
+              dst[1] = o[1];
+            }
           }
           sword |= uint32_t(code) << (8 * c);
         }
@@ -540,9 +557,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + row * p.d + nt * BN + 128 * half +
                                                 32 * c);
+          if (p.out32) {
+            st_global_32B(dst, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+            st_global_32B(dst + 2, o[8], o[9], o[10], o[11], o[12], o[13], o[14], o[15]);
+          } else {
 #pragma unroll
-          for (int w = 0; w < 4; ++w)
-            dst[w] = make_uint4(o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
+            for (int w = 0; w < 4; ++w)
+              dst[w] = make_uint4(o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
+          }
         }
       }
     }
@@ -705,6 +727,7 @@ cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int*
   p.out_q = hq;
   p.out_sf = hs;
   p.status = status;
+  p.out32 = (reinterpret_cast<uintptr_t>(hq) & 31u) == 0;
   return launch_mode<0>(p, ta, tb, st);
 }
 
@@ -732,6 +755,7 @@ cudaError_t launch_gemm_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs, const
   p.out_q = hq;
   p.out_sf = hs;
   p.status = status;
+  p.out32 = (reinterpret_cast<uintptr_t>(hq) & 31u) == 0;
   if (hs_layout == kScalesGroup32) return launch_mode<0, true, kScalesGroup32>(p, ta, tb, st);
   return launch_mode<0, true, kScalesTiled128>(p, ta, tb, st);
 }
@@ -757,6 +781,7 @@ cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* coun
   p.rows_capacity = rows_capacity;
   p.out_bf16 = yp;
   p.status = status;
+  p.out32 = (reinterpret_cast<uintptr_t>(yp) & 31u) == 0;
   return launch_mode<1>(p, ta, tb, st);
 }
 

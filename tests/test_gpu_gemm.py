@@ -78,15 +78,17 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("out_off", [0, 16])   # bytes: 32-byte-aligned output, or 16 only
 @pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("sizes,d,I", CASES)
-def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel):
+def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel, out_off):
     counts, offsets, rows, rc = _groups(sizes, kernel)
     E = len(sizes)
     W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=1)
     xq = synth.random_e4m3_codes((rc, d), seed=2).numpy()
     xs = synth.random_scale_codes((rc, d // 32), lo=118, hi=130, seed=3).numpy()
-    hq = torch.full((rc, I), 0x5A, dtype=torch.uint8, device="cuda")
+    hq = torch.full((rc * I + out_off,), 0x5A, dtype=torch.uint8, device="cuda")[out_off:]
+    hq = hq.view(rc, I)
     hs = torch.full((abi.moe_activation_scale_bytes(rc, I, kernel - 1),), 0x5A,
                     dtype=torch.uint8, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
@@ -108,15 +110,17 @@ def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel):
     assert np.all(got_c[pad_rows] == 0x5A) and np.all(got_s[pad_rows] == 0x5A)
 
 
+@pytest.mark.parametrize("out_off", [0, 16])   # bytes: 32-byte-aligned output, or 16 only
 @pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("sizes,d,I", CASES)
-def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I, kernel):
+def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I, kernel, out_off):
     counts, offsets, rows, rc = _groups(sizes, kernel)
     E = len(sizes)
     W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=4)
     hq = synth.random_e4m3_codes((rc, I), seed=5).numpy()
     hs = synth.random_scale_codes((rc, I // 32), lo=118, hi=130, seed=6).numpy()
-    yp = torch.full((rc, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    yp = torch.full((rc * d + out_off // 2,), 7.0, dtype=torch.bfloat16, device="cuda")
+    yp = yp[out_off // 2:].view(rc, d)
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     abi.moe_grouped_gemm_w2(_dev(hq), _dev(_act_scales(hs, I, kernel)), _dev(counts),
                             _dev(offsets), E, I, d,
