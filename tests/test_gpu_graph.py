@@ -67,3 +67,28 @@ def test_host_pipeline_matches_forward(abi):
     assert abi.moe_check_device_status(pipe.ws) == 0
     for got, ref in zip(outs, want):
         assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("name,n,a4w4", [("decode_t64", 60, False), ("decode_t64", 30, True),
+                                         ("prefill_skewed_t8192", 10, False)])
+def test_repeated_forwards_bit_identical(abi, name, n, a4w4):
+    """Back-to-back forwards, eager and replayed as a graph, give the first
+    forward's output bit for bit. Consecutive kernels overlap through
+    programmatic dependent launch; a missing wait would show up here as a
+    difference between repetitions."""
+    wl = synth.workload(name)
+    L = synth.make_layer(wl, seed=3, device="cuda")
+    layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k)
+    ws = layer.workspace(wl.T)
+    ref = layer.forward(L["x"], L["logits"], ws=ws, a4w4=a4w4).clone()
+    y = torch.empty_like(ref)
+    diffs = 0
+    for _ in range(n):
+        layer.forward(L["x"], L["logits"], ws=ws, y=y, a4w4=a4w4)
+        diffs += int(not torch.equal(y.view(torch.int16), ref.view(torch.int16)))
+    graph, yg, wsg = layer.capture(L["x"], L["logits"], a4w4=a4w4)
+    for _ in range(n):
+        graph.replay()
+        diffs += int(not torch.equal(yg.view(torch.int16), ref.view(torch.int16)))
+    assert diffs == 0
+    assert abi.moe_check_device_status(ws) == 0 and abi.moe_check_device_status(wsg) == 0
