@@ -1,23 +1,27 @@
-"""Benchmark of the MXFP4 latent-MoE layer on GB300 (one JSON line on rank 0).
+"""Benchmark of the MXFP4 latent-MoE layer on one GB300 (one JSON line).
 
 One step = one pass of the whole layer (route, group, quantise, stage-1 GEMM
 + GLU + requant, stage-2 GEMM, combine) over one batch of synthetic tokens of
-the chosen workload (default decode_t64: T=64, d=3584, E=896, k=16, I=3072).
+the chosen workload. The headline is the largest workload,
+prefill_outlier_t32768 (T=32768, d=3584, E=896, k=16, I=3072, 1% of the rows
+scaled by 64); the other full-size workloads are measured in the same run and
+reported under per_workload.
 
   value      tokens/s, device-timed with CUDA events around K moe_forward
-             calls, inputs resident in HBM (max over ranks; N ranks run
-             independent replicas of the workload).
+             calls, inputs resident in HBM.
   e2e        the same metric through the layer's HostPipeline: every step's
              inputs copied from pinned host memory and its output read back,
              the copies on two copy streams overlapping the neighbouring
-             steps' forwards (e2e_serial: the same in one stream).
+             steps' forwards (e2e_serial: the same in one stream; e2e_graph:
+             serial copies around a replayed CUDA graph of the step).
   roofline   the dominant kernel: algorithmic bytes (HBM-bound workloads) or
              FLOPs (tensor-bound) per launch / its mean event-timed duration,
              against MEASURED_PEAKS.json.
   cpu_baseline  the CPU oracle (test infrastructure) timed on the host cores on
-             a bounded sample of the same workload (rank 0, N=1 only).
+             a bounded sample of the headline workload.
 
---impl reference runs the oracle itself as the reference arm.
+The layer runs on one GPU; --gpus other than 1 is refused before any GPU
+work. --impl reference runs the oracle itself as the reference arm.
 """
 import argparse
 import hashlib
@@ -43,13 +47,23 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio: kind::mxf4 (A4W4 stage 1) ru
 FP4_MMA_OVER_BF16 = 2 * FP8_OVER_BF16
 
 
+# The other full-size workloads, measured in the same run as the headline:
+# the two decode batches, the skewed prefill, and the A4W4 stage 1 at prefill.
+DEFAULT_PER_WORKLOAD = ("decode_t64,decode_t512,prefill_skewed_t8192,"
+                        "prefill_skewed_t8192:a4w4,prefill_outlier_t32768:a4w4")
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode_t64")
+    ap.add_argument("--workload", default="prefill_outlier_t32768",
+                    help="headline workload (default: the largest, T=32768)")
+    ap.add_argument("--per-workload", default=DEFAULT_PER_WORKLOAD,
+                    help="comma list of further workloads measured in the same run "
+                         "(name or name:a4w4; 'none' for none)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override: T tokens at the full layer dims, uniform routing")
     ap.add_argument("--seed", type=int, default=0)
@@ -117,10 +131,13 @@ class ClockSampler:
         if self.thread:
             self.thread.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Clocks over [t0, t1] (wall-clock seconds; default: the first to the
+        last mark), padded by one sampling period on each side."""
         if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, 1e30)
+        if t0 is None:
+            t0, t1 = (self.marks[0], self.marks[-1]) if len(self.marks) >= 2 else (0, 1e30)
         rows = [r for t, r in self.rows if t0 - 0.25 <= t <= t1 + 0.25] or [r for _, r in self.rows]
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
@@ -206,10 +223,8 @@ def oracle_seconds(wl, host, threads, a4w4=False):
 
 
 def run_reference(args, wl):
-    from mxfp4_latent_moe_gb300 import replicas
-    rank, world, _ = replicas.dist_env()
-    if rank != 0:
-        return
+    if int(os.environ.get("RANK", "0")) != 0:
+        return   # under torchrun only rank 0 runs the (CPU) reference arm
     import torch
     from mxfp4_latent_moe_gb300 import synth
     import oracle
@@ -354,31 +369,24 @@ def run_step(args, wl):
     print(json.dumps(line))
 
 
-def main():
-    args = parse()
-    from mxfp4_latent_moe_gb300 import synth
-    wl = synth.workload(args.workload) if args.tokens <= 0 else synth.full_dims(args.tokens)
-    if args.impl == "reference":
-        return run_reference(args, wl)
-    if args.step:
-        return run_step(args, wl)
-
+def _free(*objs):
     import torch
-    from mxfp4_latent_moe_gb300 import replicas
-    rank, world, local = replicas.dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
+    for o in objs:
+        del o
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
-    import __graft_entry__
-    __graft_entry__.build()
-    from mxfp4_latent_moe_gb300 import abi
+
+def measure_layer(args, wl, dev, sampler, a4w4=False):
+    """Builds the workload's layer on `dev` and times it: K moe_forward calls on
+    device-resident inputs (one CUDA-event pair), then the same kernels through
+    the step entry points with events between them. Returns (entry, state):
+    the per-workload JSON entry and the device objects the headline reuses."""
+    import torch
+    from mxfp4_latent_moe_gb300 import abi, synth
     from mxfp4_latent_moe_gb300.layer import MoeLayer
 
-    L = synth.make_layer(wl, seed=replicas.replica_seed(args.seed, rank), device=dev)
+    L = synth.make_layer(wl, seed=args.seed, device=dev)
     kernel_arg = {"auto": abi.GEMM_AUTO, "token": abi.GEMM_TOKEN_TILES,
                   "weight": abi.GEMM_WEIGHT_TILES}[args.gemm_kernel]
     layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k, kernel=kernel_arg)
@@ -391,24 +399,23 @@ def main():
     stream = torch.cuda.current_stream()
 
     def fwd():
-        layer.forward(x, logits, ws=ws, y=y, topk_ids=ids, topk_w=w, a4w4=args.a4w4)
+        layer.forward(x, logits, ws=ws, y=y, topk_ids=ids, topk_w=w, a4w4=a4w4)
 
     # routing statistics for the roofline (outside any timed region)
     fwd()
     if abi.moe_check_device_status(ws) != abi.OK:
-        raise RuntimeError("device status error in the first forward")
+        raise RuntimeError("device status error in the first forward (%s)" % wl.name)
     counts = torch.bincount(ids.reshape(-1).long(), minlength=E)
     U = int((counts > 0).sum())
     valid_rows = T * k
-    kernel = layer.kernel_for(T)      # both stages, or stage 2 under --a4w4
-    pad = 32 if kernel == abi.GEMM_WEIGHT_TILES and not args.a4w4 else 128
+    kernel = layer.kernel_for(T)      # both stages, or stage 2 under a4w4
+    pad = 32 if kernel == abi.GEMM_WEIGHT_TILES and not a4w4 else 128
     layout = abi.SCALES_GROUP32 if kernel == abi.GEMM_WEIGHT_TILES else abi.SCALES_TILED128
-    xs_layout = abi.SCALES_TILED128 if args.a4w4 else layout
+    xs_layout = abi.SCALES_TILED128 if a4w4 else layout
     rows_cap = abi.moe_rows_capacity(T, E, k, pad)
     padded_rows = int(((counts + pad - 1) // pad * pad).sum())
     expert_bytes = layer.weight_bytes_per_expert()
     w13_bytes = 2 * I * d // 2 + 2 * I * d // 32
-    w2_bytes = d * I // 2 + d * I // 32
     flops = 6.0 * T * k * d * I
     l2_note = "inputs larger than L2 (touched weights %.2f GB)" % (U * expert_bytes / 1e9)
     flush = None
@@ -416,15 +423,13 @@ def main():
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
         l2_note = "L2 flushed between steps (256 MB write)"
 
-    sampler = ClockSampler(local)
-    sampler.start()
     for _ in range(max(3, args.warmup)):
         fwd()
     torch.cuda.synchronize()
 
     # ---- timed region: K moe_forward calls on device-resident inputs
-    replicas.barrier()
     torch.cuda.synchronize()
+    t_wall0 = time.time()
     sampler.mark()
     if flush is None:
         t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -444,8 +449,9 @@ def main():
         torch.cuda.synchronize()
         total_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps))
     sampler.mark()
-    total_ms = replicas.max_over_ranks(total_ms, dev)
-    replicas.barrier()
+    t_wall1 = time.time()
+    if abi.moe_check_device_status(ws) != abi.OK:
+        raise RuntimeError("device status error in the timed forwards (%s)" % wl.name)
     # this library's kernels per forward: route, grouping (one kernel for a
     # one-chunk batch of T <= 256 tokens, else count + scan + scatter),
     # quantisation, the two GEMMs, combine
@@ -458,16 +464,16 @@ def main():
     s2r = torch.empty(T * k, dtype=torch.int32, device=dev)
     r2s = torch.empty(rc, dtype=torch.int32, device=dev)
     pws = torch.zeros(abi.moe_permute_workspace_size(T, E), dtype=torch.uint8, device=dev)
-    xq = torch.empty(rc, d // 2 if args.a4w4 else d, dtype=torch.uint8, device=dev)
+    xq = torch.empty(rc, d // 2 if a4w4 else d, dtype=torch.uint8, device=dev)
     xs = torch.empty(abi.moe_activation_scale_bytes(rc, d, xs_layout), dtype=torch.uint8,
                      device=dev)
     hq = torch.empty(rc, I, dtype=torch.uint8, device=dev)
     hs = torch.empty(abi.moe_activation_scale_bytes(rc, I, layout), dtype=torch.uint8, device=dev)
     yp = torch.empty(rc, d, dtype=torch.bfloat16, device=dev)
     gws = torch.zeros(256, dtype=torch.uint8, device=dev)
-    names = ["route_topk", "permute", "quant_mxfp4" if args.a4w4 else "quant_mxfp8",
+    names = ["route_topk", "permute", "quant_mxfp4" if a4w4 else "quant_mxfp8",
              "gemm_w13_glu", "gemm_w2", "combine"]
-    if args.a4w4:
+    if a4w4:
         quant_call = lambda: abi.moe_quant_mxfp4(x, T, d, s2r, k, xq, xs, rc, xs_layout)
         w13_call = lambda: abi.moe_grouped_gemm_w13_glu_a4w4(
             xq, xs, counts_d, offsets_d, E, d, I, layout, layer.w13, layer.w13_sf, hq, hs, rc, gws)
@@ -499,13 +505,87 @@ def main():
             c()
             kev[i][j + 1].record(stream)
     torch.cuda.synchronize()
-    sampler.mark()
     kms = {n: statistics.mean(kev[i][j].elapsed_time(kev[i][j + 1]) for i in range(args.steps))
            for j, n in enumerate(names)}
     if abi.moe_check_device_status(gws) != abi.OK or abi.moe_check_device_status(pws) != abi.OK:
-        raise RuntimeError("device status error in the kernel breakdown")
+        raise RuntimeError("device status error in the kernel breakdown (%s)" % wl.name)
 
-    # ---- end to end through the public API: pinned host in, host out, every step
+    peaks, peak_src = load_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    bf16_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    tensor_peak = bf16_peak * FP8_OVER_BF16
+    w13_peak = bf16_peak * (FP4_OVER_BF16 if a4w4 else FP8_OVER_BF16)
+    t_mem = U * expert_bytes / (hbm_peak * 1e9)
+    t_math = 4.0 * T * k * d * I / (w13_peak * 1e12) + 2.0 * T * k * d * I / (tensor_peak * 1e12)
+    bound = "hbm" if t_mem >= t_math else "tensor"
+    ms_per_step = total_ms / args.steps
+    layer_frac = max(t_mem, t_math) / (ms_per_step / 1e3)
+    family = "weight_tiles" if kernel == abi.GEMM_WEIGHT_TILES else "token_tiles"
+    dom = "gemm_w13_glu"
+    dom_s = kms[dom] / 1e3
+    x_row_bytes = (d // 2 if a4w4 else d) + d // 32
+    if bound == "hbm":
+        dom_bytes = U * w13_bytes + valid_rows * x_row_bytes + valid_rows * (I + I // 32)
+        roof = {"kernel": dom, "bound": "hbm", "achieved": dom_bytes / dom_s / 1e9,
+                "peak": hbm_peak, "unit": "GB/s", "frac": dom_bytes / dom_s / 1e9 / hbm_peak,
+                "traffic": profiled_traffic(dom, wl.name, family) if not a4w4 else None,
+                "algorithmic_bytes": dom_bytes,
+                "algorithmic_bytes_how": "touched experts x w13 bytes (codes + scales) + "
+                                         "T*k x-code rows in + T*k h-code rows out",
+                "mean_ms": kms[dom], "peak_source": peak_src + " hbm_gbs (copy)"}
+    else:
+        dom_flops = 4.0 * T * k * d * I
+        ratio, what = (FP4_OVER_BF16, "fp4") if a4w4 else (FP8_OVER_BF16, "fp8")
+        roof = {"kernel": dom, "bound": "tensor", "achieved": dom_flops / dom_s / 1e12,
+                "peak": w13_peak, "unit": "TFLOP/s",
+                "frac": dom_flops / dom_s / 1e12 / w13_peak,
+                "frac_of_sustained": dom_flops / dom_s / 1e12 / (bf16_sus * ratio),
+                "traffic": profiled_traffic(dom, wl.name, family) if not a4w4 else None,
+                "algorithmic_flops": dom_flops,
+                "algorithmic_flops_how": "4*T*k*d*I (gate and up products of the routed rows; "
+                                         "padding rows not credited)",
+                "mean_ms": kms[dom],
+                "peak_source": peak_src + " bf16_tflops (burst) x %.1f (nominal %s / bf16 dense "
+                               "ratio)" % (ratio, what)}
+        if a4w4:
+            mma_peak = bf16_peak * FP4_MMA_OVER_BF16
+            roof["frac_of_measured_mma_rate"] = dom_flops / dom_s / 1e12 / mma_peak
+            roof["measured_mma_rate_peak"] = mma_peak
+    entry = {
+        "workload": wl.name, "a4w4": bool(a4w4),
+        "value": T * args.steps / (total_ms / 1e3), "unit": "tokens/s",
+        "ms_per_step": ms_per_step, "steps": args.steps,
+        "gemm_kernel": family, "touched_experts": U, "padded_rows": padded_rows,
+        "layer_roofline": {"bound": bound, "time_ms": 1e3 * max(t_mem, t_math),
+                           "frac": layer_frac,
+                           "frac_of_sustained": (max(t_mem, t_math) if bound == "hbm" else
+                                                 t_math * bf16_peak / bf16_sus)
+                           / (ms_per_step / 1e3),
+                           "tflops": flops / (ms_per_step / 1e3) / 1e12,
+                           "weight_gbs": U * expert_bytes / (ms_per_step / 1e3) / 1e9,
+                           "how": "max(touched experts x 17,547,264 B / hbm_gbs, 4TkdI FLOP / "
+                                  "stage-1 peak + 2TkdI FLOP / (bf16_tflops x 2))"},
+        "roofline": roof,
+        "kernels_ms": kms,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "l2": l2_note,
+    }
+    state = dict(L=L, layer=layer, ws=ws, y=y, flush=flush, stream=stream)
+    return entry, state
+
+
+def measure_e2e(args, wl, st, a4w4=False):
+    """The headline's end-to-end legs through the public API: every step's x and
+    logits copied from pinned host memory and y copied back (HostPipeline, the
+    copies on copy streams; serial, in one stream; graph-replayed)."""
+    import torch
+    from mxfp4_latent_moe_gb300 import abi
+    from mxfp4_latent_moe_gb300.layer import HostPipeline
+    L, layer, ws, y, flush, stream = (st[n] for n in ("L", "layer", "ws", "y", "flush", "stream"))
+    T, d = wl.T, wl.d
+    x, logits = L["x"], L["logits"]
     x_h = x.cpu().pin_memory()
     lg_h = logits.cpu().pin_memory()
     y_h = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
@@ -514,7 +594,7 @@ def main():
     for _ in range(3):
         x_d.copy_(x_h, non_blocking=True)
         lg_d.copy_(lg_h, non_blocking=True)
-        layer.forward(x_d, lg_d, ws=ws, y=y, a4w4=args.a4w4)
+        layer.forward(x_d, lg_d, ws=ws, y=y, a4w4=a4w4)
         y_h.copy_(y, non_blocking=True)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -524,17 +604,13 @@ def main():
             flush.fill_(i & 0xFF)
         x_d.copy_(x_h, non_blocking=True)
         lg_d.copy_(lg_h, non_blocking=True)
-        layer.forward(x_d, lg_d, ws=ws, y=y, a4w4=args.a4w4)
+        layer.forward(x_d, lg_d, ws=ws, y=y, a4w4=a4w4)
         y_h.copy_(y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    sampler.stop()
-    e2e_serial_ms = replicas.max_over_ranks(e0.elapsed_time(e1), dev)
+    e2e_serial_ms = e0.elapsed_time(e1)
 
-    # ---- the same copies through HostPipeline: batch i+1's inputs and batch
-    # i-1's output cross on copy streams while batch i computes
-    from mxfp4_latent_moe_gb300.layer import HostPipeline
-    pipe = HostPipeline(layer, T, a4w4=args.a4w4)
+    pipe = HostPipeline(layer, T, a4w4=a4w4)
     for _ in range(3):
         pipe.submit(x_h, lg_h, y_h)
     pipe.synchronize()
@@ -551,10 +627,10 @@ def main():
     torch.cuda.synchronize()
     if abi.moe_check_device_status(pipe.ws) != abi.OK:
         raise RuntimeError("device status error in the pipelined end-to-end steps")
-    e2e_ms = replicas.max_over_ranks(p0.elapsed_time(p1), dev)
+    e2e_ms = p0.elapsed_time(p1)
+    del pipe
 
-    # ---- the same end to end with the step captured as one CUDA graph
-    graph, y_g, _ = layer.capture(x_d, lg_d, ws=ws, a4w4=args.a4w4)
+    graph, y_g, _ = layer.capture(x_d, lg_d, ws=ws, a4w4=a4w4)
     for _ in range(3):
         graph.replay()
     torch.cuda.synchronize()
@@ -569,94 +645,118 @@ def main():
         y_h.copy_(y_g, non_blocking=True)
     g1.record(stream)
     torch.cuda.synchronize()
-    e2e_graph_ms = replicas.max_over_ranks(g0.elapsed_time(g1), dev)
+    e2e_graph_ms = g0.elapsed_time(g1)
     if abi.moe_check_device_status(ws) != abi.OK:
         raise RuntimeError("device status error in the graph replays")
+    del graph
+    rate = lambda ms: T * args.steps / (ms / 1e3)
+    return {
+        "e2e": {"value": rate(e2e_ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * d * 2 + T * wl.E * 4,
+                "d2h_bytes_per_step": T * d * 2,
+                "how": "HostPipeline: pinned host batches, copies on two copy streams "
+                       "overlapping the neighbouring batches' forwards"},
+        "e2e_serial": {"value": rate(e2e_serial_ms), "unit": "tokens/s",
+                       "how": "same copies and forwards in one stream"},
+        "e2e_graph": {"value": rate(e2e_graph_ms), "unit": "tokens/s",
+                      "how": "same copies, the step replayed as one CUDA graph "
+                             "(MoeLayer.capture)"},
+    }
 
-    peaks, peak_src = load_peaks()
-    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    tensor_peak = bf16_peak * FP8_OVER_BF16
-    w13_peak = bf16_peak * (FP4_OVER_BF16 if args.a4w4 else FP8_OVER_BF16)
-    t_mem = U * expert_bytes / (hbm_peak * 1e9)
-    t_math = 4.0 * T * k * d * I / (w13_peak * 1e12) + 2.0 * T * k * d * I / (tensor_peak * 1e12)
-    bound = "hbm" if t_mem >= t_math else "tensor"
-    ms_per_step = total_ms / args.steps
-    layer_frac = max(t_mem, t_math) / (ms_per_step / 1e3)
-    family = "weight_tiles" if kernel == abi.GEMM_WEIGHT_TILES else "token_tiles"
-    dom = "gemm_w13_glu"
-    dom_s = kms[dom] / 1e3
-    x_row_bytes = (d // 2 if args.a4w4 else d) + d // 32
-    if bound == "hbm":
-        dom_bytes = U * w13_bytes + valid_rows * x_row_bytes + valid_rows * (I + I // 32)
-        roof = {"kernel": dom, "bound": "hbm", "achieved": dom_bytes / dom_s / 1e9,
-                "peak": hbm_peak, "unit": "GB/s", "frac": dom_bytes / dom_s / 1e9 / hbm_peak,
-                "traffic": profiled_traffic(dom, wl.name, family) if not args.a4w4 else None,
-                "algorithmic_bytes": dom_bytes, "peak_source": peak_src}
+
+def cpu_baseline_leg(args, wl, L, a4w4=False, budget_s=15.0):
+    """The oracle, as it stands, on the host cores, on the first n tokens of
+    the workload, n sized for about budget_s seconds of CPU work."""
+    cores = os.cpu_count() or 1
+    if args.cpu_sample:
+        n = args.cpu_sample
     else:
-        dom_flops = 4.0 * T * k * d * I
-        ratio, what = (FP4_OVER_BF16, "fp4") if args.a4w4 else (FP8_OVER_BF16, "fp8")
-        roof = {"kernel": dom, "bound": "tensor", "achieved": dom_flops / dom_s / 1e12,
-                "peak": w13_peak, "unit": "TFLOP/s",
-                "frac": dom_flops / dom_s / 1e12 / w13_peak,
-                "traffic": profiled_traffic(dom, wl.name, family) if not args.a4w4 else None,
-                "algorithmic_flops": dom_flops,
-                "peak_source": peak_src + " bf16 x %.1f (%s / bf16 nominal ratio)" % (ratio, what)}
-        if args.a4w4:
-            mma_peak = bf16_peak * FP4_MMA_OVER_BF16
-            roof["frac_of_measured_mma_rate"] = dom_flops / dom_s / 1e12 / mma_peak
-            roof["measured_mma_rate_peak"] = mma_peak
+        n0 = min(wl.T, cores)
+        per_token = oracle_seconds(wl, oracle_inputs(L, n0), cores, a4w4) / n0
+        n = max(1, min(wl.T, int(budget_s / per_token)))
+    dt = oracle_seconds(wl, oracle_inputs(L, n), cores, a4w4=a4w4)
+    return {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "first %d of %d tokens of the workload, full layer (%.1f s)" % (n, wl.T, dt),
+            "cpu_model": cpu_model()}
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n = args.cpu_sample or (T if T <= 64 else 32)
-        cores = os.cpu_count() or 1
-        dt = oracle_seconds(wl, oracle_inputs(L, n), cores, a4w4=args.a4w4)
-        cpu = {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": "first %d of %d tokens, full layer (%.1f s)" % (n, T, dt),
-               "cpu_model": cpu_model()}
 
-    if rank == 0:
-        line = {
-            "metric": METRIC,
-            "value": replicas.aggregate_rate(T, world, args.steps, total_ms),
-            "unit": "tokens/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": ("stage1 mxfp4(e2m1)xmxfp4(e2m1)->f32, stage2 mxfp8(e4m3)xmxfp4(e2m1)->f32"
-                      if args.a4w4 else "mxfp8(e4m3)xmxfp4(e2m1)->f32"),
-            "data": "synthetic (seeded; x~N(0,1) bf16, logits~N(0,1), uniform E2M1 codes, "
-                    "E8M0 scales 118..122)",
-            "config": {"workload": wl.name, "T": T, "d": d, "E": E, "k": k, "I": I,
-                       "gemm_kernel": "weight_tiles" if kernel == abi.GEMM_WEIGHT_TILES
-                       else "token_tiles", "a4w4": bool(args.a4w4),
-                       "touched_experts": U, "padded_rows": padded_rows,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": l2_note},
-            "layer_roofline": {"bound": bound, "time_ms": 1e3 * max(t_mem, t_math),
-                               "frac": layer_frac, "tflops": flops / (ms_per_step / 1e3) / 1e12,
-                               "weight_gbs": U * expert_bytes / (ms_per_step / 1e3) / 1e9},
-            "roofline": roof,
-            "kernels_ms": kms,
-            "gpu_launches": launches_per_step * args.steps,
-            "e2e": {"value": replicas.aggregate_rate(T, world, args.steps, e2e_ms),
-                    "unit": "tokens/s",
-                    "h2d_bytes_per_step": T * d * 2 + T * E * 4,
-                    "d2h_bytes_per_step": T * d * 2,
-                    "how": "HostPipeline: pinned host batches, copies on two copy streams "
-                           "overlapping the neighbouring batches' forwards"},
-            "e2e_serial": {"value": replicas.aggregate_rate(T, world, args.steps, e2e_serial_ms),
-                           "unit": "tokens/s", "how": "same copies and forwards in one stream"},
-            "e2e_graph": {"value": replicas.aggregate_rate(T, world, args.steps, e2e_graph_ms),
-                          "unit": "tokens/s", "how": "same copies, the step replayed as one "
-                          "CUDA graph (MoeLayer.capture)"},
-            "cpu_baseline": cpu,
-            "clocks": sampler.summary(),
-        }
-        print(json.dumps(line))
-    if world > 1:
-        torch.distributed.destroy_process_group()
+def parse_per_workload(spec):
+    out = []
+    for item in (spec or "").split(","):
+        item = item.strip()
+        if not item or item == "none":
+            continue
+        name, _, mode = item.partition(":")
+        out.append((name, mode == "a4w4"))
+    return out
+
+
+def main():
+    args = parse()
+    from mxfp4_latent_moe_gb300 import synth
+    wl = synth.workload(args.workload) if args.tokens <= 0 else synth.full_dims(args.tokens)
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != 1 or world != 1:
+        # libmoe.so is single-GPU code: its prefill GEMMs multicast TMA loads
+        # inside 2-CTA clusters, which may only run in one-GPU programs.
+        sys.stderr.write("bench.py: this layer runs on one GPU only (--gpus 1); "
+                         "got --gpus %d, WORLD_SIZE %d\n" % (args.gpus, world))
+        sys.exit(2)
+    if args.step:
+        return run_step(args, wl)
+
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+
+    sampler = ClockSampler(0)
+    sampler.start()
+    head, st = measure_layer(args, wl, dev, sampler, a4w4=args.a4w4)
+    e2e = measure_e2e(args, wl, st, a4w4=args.a4w4)
+    cpu = None if args.no_cpu_baseline else cpu_baseline_leg(args, wl, st["L"], a4w4=args.a4w4)
+    st.clear()
+    _free()
+    per = {}
+    for name, a4 in parse_per_workload(args.per_workload):
+        if name == wl.name and a4 == bool(args.a4w4):
+            continue
+        entry, st2 = measure_layer(args, synth.workload(name), dev, sampler, a4w4=a4)
+        st2.clear()
+        _free()
+        per[name + (":a4w4" if a4 else "")] = entry
+    sampler.stop()
+
+    line = {
+        "metric": METRIC,
+        "value": head["value"], "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": ("stage1 mxfp4(e2m1)xmxfp4(e2m1)->f32, stage2 mxfp8(e4m3)xmxfp4(e2m1)->f32"
+                  if args.a4w4 else "mxfp8(e4m3)xmxfp4(e2m1)->f32"),
+        "data": "synthetic (seeded; x~N(0,1) bf16, logits~N(0,1), uniform E2M1 codes, "
+                "E8M0 scales 118..122)",
+        "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "I": wl.I,
+                   "gemm_kernel": head["gemm_kernel"], "a4w4": bool(args.a4w4),
+                   "touched_experts": head["touched_experts"],
+                   "padded_rows": head["padded_rows"], "parallelism": "single",
+                   "l2": head["l2"]},
+        "layer_roofline": head["layer_roofline"],
+        "roofline": head["roofline"],
+        "kernels_ms": head["kernels_ms"],
+        "gpu_launches": head["gpu_launches"],
+        "e2e": e2e["e2e"],
+        "e2e_serial": e2e["e2e_serial"],
+        "e2e_graph": e2e["e2e_graph"],
+        "cpu_baseline": cpu,
+        "clocks": head["clocks"],
+        "per_workload": per,
+    }
+    print(json.dumps(line))
 
 
 if __name__ == "__main__":

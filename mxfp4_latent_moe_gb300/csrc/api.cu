@@ -8,8 +8,10 @@ namespace {
 
 using moe::tiled_sf_offset;
 
-constexpr int kMaxE = 1024;
-constexpr int kMaxK = 32;
+using moe::check_routing_shape;
+using moe::pow2_in;
+constexpr int kMaxE = moe::kMaxExperts;
+constexpr int kMaxK = moe::kMaxTopK;
 // Expert groups: multiples of 128 rows for token tiles, of 32 for weight tiles
 // (whose activation scales use the GROUP32 layout).
 int32_t group_pad(int32_t kernel) { return kernel == MOE_GEMM_WEIGHT_TILES ? 32 : 128; }
@@ -38,21 +40,10 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-moe_status check_routing_shape(int32_t T, int32_t E, int32_t k) {
-  if (T < 0 || E < 0 || k < 0) return MOE_ERR_INVALID_ARGUMENT;
-  if (E < 1 || E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED;
-  if (int64_t(T) * k >= int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
-  return MOE_OK;
-}
-
 moe_status check_width(int32_t w) {
   if (w < 0) return MOE_ERR_INVALID_ARGUMENT;
   if (w < 128 || w % 128 != 0 || w > (1 << 20)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
-}
-
-bool pow2_in(int32_t v, int32_t lo, int32_t hi) {
-  return v >= lo && v <= hi && (v & (v - 1)) == 0;
 }
 
 int64_t rows_capacity_of(int32_t T, int32_t E, int32_t k, int32_t pad_m) {

@@ -2,9 +2,29 @@
 // Arguments are validated by the C-ABI layer (api.cu) before they get here.
 #pragma once
 
+#include <climits>
+
 #include "common.cuh"
 
 namespace moe {
+
+// Shape limits of every routing and grouping entry point: E experts (one
+// thread per expert in the grouping scans and in the GEMMs' tile prefix) and
+// k selected experts per token (one lane per selected expert in routing).
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+inline moe_status check_routing_shape(int32_t T, int32_t E, int32_t k) {
+  if (T < 0 || E < 0 || k < 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (E < 1 || E > kMaxExperts || k > kMaxTopK || k > E) return MOE_ERR_UNSUPPORTED;
+  if (int64_t(T) * k >= int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// v is a power of two in [lo, hi].
+inline bool pow2_in(int32_t v, int32_t lo, int32_t hi) {
+  return v >= lo && v <= hi && (v & (v - 1)) == 0;
+}
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int* ids, float* w,
                               cudaStream_t st);

@@ -157,9 +157,11 @@ __global__ void __launch_bounds__(kChunk) permute_scatter_kernel(
 
 // Batches of one chunk (T <= 256, decode): histogram, scan and scatter in
 // one block of 1024 threads, row_to_slot filled with -1 first (one launch
-// instead of three and a memset). Threads 0..255 own the tokens (same masks
-// and ranks as the three kernels above); all 1024 share the fill, the mask
-// clearing and the scan (one expert per thread, E <= 1024).
+// instead of three and a memset). Only the launch itself overlaps the
+// previous kernel; the fill runs after griddepcontrol.wait. Threads 0..255
+// own the tokens (same masks and ranks as the three kernels above); all 1024
+// share the fill, the mask clearing and the scan (one expert per thread,
+// E <= 1024).
 constexpr int kSingleThreads = 1024;
 
 __global__ void __launch_bounds__(kSingleThreads)
@@ -172,7 +174,12 @@ __global__ void __launch_bounds__(kSingleThreads)
   __shared__ int warp_sums[kSingleThreads / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();
-  {   // row_to_slot is written by no kernel before this one: filled before the wait
+  // Everything below waits for the previous kernel in the stream: a library
+  // kernel launched before this one may still read or write row_to_slot
+  // (another grouping call on the same buffers, or a kernel still using
+  // memory the caller has since handed over as row_to_slot).
+  pdl_wait();
+  {
     int64_t done = 0;
     if ((reinterpret_cast<uintptr_t>(row_to_slot) & 15u) == 0) {
       int4* r4 = reinterpret_cast<int4*>(row_to_slot);
@@ -291,7 +298,10 @@ cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* 
 // the histograms live in the fixed device array below, part of this library's
 // image: every GPU that loads the library holds its 1 MiB until the process
 // exits. Its device address is looked up once per device (the first call on
-// that device, with that device current) and cached.
+// that device, with that device current) and cached for the life of the
+// process, keyed by device ordinal: callers that reset a device
+// (cudaDeviceReset) or drive it through a non-primary context are not
+// supported by this entry point.
 // ---------------------------------------------------------------------------
 namespace moe {
 
@@ -328,10 +338,10 @@ extern "C" moe_status moe_permute_noalloc(const int32_t* topk_ids, int32_t T, in
                                           int32_t* slot_to_row, int32_t* row_to_slot,
                                           int64_t rows_capacity, int32_t* status,
                                           cudaStream_t stream) {
-  if (T < 0 || E < 0 || k < 0 || rows_capacity < 0) return MOE_ERR_INVALID_ARGUMENT;
-  if (E < 1 || E > 1024 || k > 32 || k > E || int64_t(T) * k >= int64_t(INT32_MAX))
-    return MOE_ERR_UNSUPPORTED;
-  if (pad_m < 1 || pad_m > 1024 || (pad_m & (pad_m - 1)) != 0) return MOE_ERR_UNSUPPORTED;
+  if (rows_capacity < 0) return MOE_ERR_INVALID_ARGUMENT;
+  const moe_status shape = moe::check_routing_shape(T, E, k);   // the rules of moe_permute
+  if (shape != MOE_OK) return shape;
+  if (!moe::pow2_in(pad_m, 1, 1024)) return MOE_ERR_UNSUPPORTED;
   if (!counts || !offsets || !moe::is_aligned4(counts) || !moe::is_aligned4(offsets))
     return MOE_ERR_INVALID_ARGUMENT;
   const bool any = T > 0 && k > 0;

@@ -29,6 +29,16 @@ def group32_index(rows, K):
     return ((r // 32) * (K // 128) + b // 4) * 512 + (r % 32) * 16 + b % 4
 
 
+def scale_offsets(rows, K, layout):
+    """Byte offsets, as a torch tensor on rows' device, of the scales of the
+    given rows (int64 tensor [n]) in layout 0 (TILED) or 1 (GROUP32): [n][K/32]."""
+    r = rows.to(torch.int64)[:, None]
+    b = torch.arange(K // 32, dtype=torch.int64, device=rows.device)[None, :]
+    if layout:
+        return ((r // 32) * (K // 128) + b // 4) * 512 + (r % 32) * 16 + b % 4
+    return ((r // 128) * (K // 128) + b // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + b % 4
+
+
 def untile_g32(buf, rows, K):
     return buf.reshape(-1)[group32_index(rows, K)]
 

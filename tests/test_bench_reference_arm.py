@@ -29,3 +29,13 @@ def test_reference_arm_json_line(orc):
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_bench_refuses_more_than_one_gpu():
+    """The layer is single-GPU code: --gpus 2 exits with an error before any
+    GPU work (no import of the CUDA library, no device touched)."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=120)
+    assert r.returncode == 2
+    assert "one GPU" in r.stderr
+    assert not [l for l in r.stdout.splitlines() if l.startswith("{")]

@@ -111,6 +111,42 @@ def test_permute_one_hot_expert_and_empty_experts(abi, orc):
     assert got["counts"][7] == T and (got["counts"] > 0).sum() == 21
 
 
+@pytest.mark.parametrize("noalloc", [False, True])
+def test_permute_back_to_back_calls_on_shared_buffers(abi, orc, noalloc):
+    """One-block grouping calls (T <= 256) enqueued back to back on the same
+    output buffers, a large batch then a small one, with no synchronisation
+    between them: the second call's -1 fill of row_to_slot must not start
+    before the first call's scatter is done, so every row past the second
+    call's groups reads -1 and its groups match the oracle."""
+    E, k, pad = 896, 16, 32
+    rng = np.random.default_rng(21)
+    big, _ = orc.route_topk(rng.normal(0, 1, (256, E)).astype(np.float32), k)
+    small, _ = orc.route_topk(rng.normal(0, 1, (8, E)).astype(np.float32), k)
+    rc = abi.moe_rows_capacity(256, E, k, pad)
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    s2r = torch.empty(256 * k, dtype=torch.int32, device="cuda")
+    r2s = torch.full((rc,), -7, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(abi.moe_permute_workspace_size(256, E), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = orc.permute(small, E, pad)
+    n = int(ref["offsets"][E])
+    d_big, d_small = torch.from_numpy(big).cuda(), torch.from_numpy(small).cuda()
+    for _ in range(10):
+        for ids, T in ((d_big, 256), (d_small, 8)):
+            if noalloc:
+                abi.moe_permute_noalloc(ids, T, E, k, pad, counts, offsets, s2r, r2s, rc, status)
+            else:
+                abi.moe_permute(ids, T, E, k, pad, counts, offsets, s2r, r2s, rc, ws)
+        torch.cuda.synchronize()
+        got = r2s.cpu().numpy()
+        assert np.array_equal(got[:n], ref["row_to_slot"])
+        assert (got[n:] == -1).all()
+        assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+        assert np.array_equal(s2r.cpu().numpy()[: 8 * k], ref["slot_to_row"])
+    assert abi.moe_check_device_status(ws) == 0 and int(status.item()) == 0
+
+
 def test_permute_flags_bad_ids_on_device(abi):
     ids = np.array([[0, 1], [2, 2], [3, 900]], np.int32)
     got = _permute_gpu(abi, ids, 8, 1, rows_capacity=128)
