@@ -72,7 +72,7 @@ def parse():
     ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "token", "weight"],
                     help="grouped-GEMM family (auto = the library's default for the shape)")
     ap.add_argument("--step", default="", choices=["", "router", "latent_down", "latent_up",
-                                                   "shared_experts"],
+                                                   "shared_experts", "block"],
                     help="time one neighbouring BF16 step at the workload's T instead of the layer")
     ap.add_argument("--a4w4", action="store_true",
                     help="MXFP4 stage-1 activations (moe_forward_a4w4); the family is stage 2's")
@@ -364,6 +364,97 @@ def run_step(args, wl):
         "cpu_baseline": {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": "%d tokens, all GEMMs of the step (%.1f s)" % (n, dt),
                          "cpu_model": cpu_model()},
+        "clocks": sampler.summary(),
+    }
+    print(json.dumps(line))
+
+
+def run_block(args, wl):
+    """Times the composed block (moe_block_forward) at the workload's T and
+    full dims: shared experts on a second stream, the same call on one stream,
+    and each part alone; reports the overlap gain."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_latent_moe_gb300 import abi, synth
+    from mxfp4_latent_moe_gb300.layer import MoeBlock
+    dev = torch.device("cuda", 0)
+    T = wl.T
+    bw = synth.block_shape("block_t%d" % T, T=T, hidden=2 * wl.d, d=wl.d, E=wl.E, k=wl.k, I=wl.I,
+                           shared_I=2 * wl.I)
+    B = synth.make_block(bw, seed=args.seed, device=dev)
+    blk = MoeBlock(B["w_down"], B["w_router"], B["w_shared13"], B["w_out"], B["w13"], B["w13_s"],
+                   B["w2"], B["w2_s"], k=bw.k)
+    ws = blk.workspace(T)
+    out = torch.empty(T, bw.hidden, dtype=torch.bfloat16, device=dev)
+    side = torch.cuda.Stream(dev)
+    stream = torch.cuda.current_stream()
+    L = blk.layer
+    # the parts, on their own buffers
+    x = torch.empty(T, bw.d, dtype=torch.bfloat16, device=dev)
+    logits = torch.empty(T, bw.E, dtype=torch.float32, device=dev)
+    ylat = torch.empty(T, bw.d, dtype=torch.bfloat16, device=dev)
+    hs = torch.empty(T, bw.shared_I, dtype=torch.bfloat16, device=dev)
+    gws = torch.zeros(max(abi.moe_gemm_bf16_workspace_size(T, n, kk, e) for n, kk, e in (
+        (bw.d, bw.hidden, 1), (bw.E, bw.hidden, 0), (2 * bw.shared_I, bw.hidden, 2),
+        (bw.hidden, bw.d + bw.shared_I, 1))), dtype=torch.uint8, device=dev)
+    lws = L.workspace(T)
+    blk.forward(B["h"], ws=ws, out=out, shared_stream=side)
+    abi.moe_gemm_bf16(B["h"], B["w_down"], T, bw.d, bw.hidden, 1, x, gws)
+    abi.moe_gemm_bf16(B["h"], B["w_router"], T, bw.E, bw.hidden, 0, logits, gws)
+    parts = {
+        "down_and_router": lambda: (
+            abi.moe_gemm_bf16(B["h"], B["w_down"], T, bw.d, bw.hidden, 1, x, gws),
+            abi.moe_gemm_bf16(B["h"], B["w_router"], T, bw.E, bw.hidden, 0, logits, gws)),
+        "routed_experts": lambda: L.forward(x, logits, ws=lws, y=ylat),
+        "shared_experts": lambda: abi.moe_gemm_bf16(B["h"], B["w_shared13"], T,
+                                                    2 * bw.shared_I, bw.hidden, 2, hs, gws),
+        "output_gemm": lambda: abi.moe_gemm_bf16_cat(ylat, bw.d, hs, bw.shared_I, B["w_out"], T,
+                                                     bw.hidden, 1, out, gws),
+        "block_one_stream": lambda: blk.forward(B["h"], ws=ws, out=out),
+        "block_two_streams": lambda: blk.forward(B["h"], ws=ws, out=out, shared_stream=side),
+    }
+    sampler = ClockSampler(0)
+    sampler.start()
+    ms = {}
+    for name, fn in parts.items():
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if name == "block_two_streams":
+            sampler.mark()
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if name == "block_two_streams":
+            sampler.mark()
+        ms[name] = e0.elapsed_time(e1) / args.steps
+    sampler.stop()
+    for w_ in (ws, gws, lws):
+        if abi.moe_check_device_status(w_) != abi.OK:
+            raise RuntimeError("device status error in the block benchmark")
+    serial_parts = sum(ms[n] for n in ("down_and_router", "routed_experts", "shared_experts",
+                                       "output_gemm"))
+    two = ms["block_two_streams"]
+    line = {
+        "metric": "latent-MoE block tokens/s (routed MXFP4 experts with BF16 latent projections, "
+                  "router and two shared experts on a second stream), 1xGB300",
+        "value": T / (two / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": two, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 dense steps, mxfp8(e4m3)xmxfp4(e2m1)->f32 routed",
+        "data": "synthetic (seeded; power-of-two grid inputs, see synth.make_block)",
+        "config": {"workload": bw.name, "T": T, "hidden": bw.hidden, "d": bw.d, "E": bw.E,
+                   "k": bw.k, "I": bw.I, "shared_I": bw.shared_I,
+                   "gemm_kernel": "weight_tiles" if L.kernel_for(T) == abi.GEMM_WEIGHT_TILES
+                   else "token_tiles",
+                   "l2": "inputs larger than L2 (routed weights)"},
+        "parts_ms": ms, "sum_of_parts_ms": serial_parts,
+        "overlap_gain_vs_one_stream": ms["block_one_stream"] / two,
+        "saved_ms_vs_sum_of_parts": serial_parts - two,
+        "gpu_launches": None,
         "clocks": sampler.summary(),
     }
     print(json.dumps(line))
@@ -704,6 +795,8 @@ def main():
         sys.stderr.write("bench.py: this layer runs on one GPU only (--gpus 1); "
                          "got --gpus %d, WORLD_SIZE %d\n" % (args.gpus, world))
         sys.exit(2)
+    if args.step == "block":
+        return run_block(args, wl)
     if args.step:
         return run_step(args, wl)
 

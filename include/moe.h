@@ -381,6 +381,82 @@ moe_status moe_router_logits(const uint16_t* x, const uint16_t* w_router, int32_
                              int32_t d_in, int32_t E, float* logits, void* ws, size_t ws_bytes,
                              cudaStream_t stream);
 
+/* C = [A1 | A2] . B^T: moe_gemm_bf16 with A given in two parts along K,
+ * a1 bf16 [M][K1] and a2 bf16 [M][K2] (each K-major, 16-byte aligned), b bf16
+ * [N][K1 + K2]; c, epilogue, ws and the split of K as moe_gemm_bf16 with
+ * K = K1 + K2 (moe_gemm_bf16_workspace_size(M, N, K1 + K2, epilogue)).
+ * K1 >= 64, K1 % 64 == 0, K2 % 64 == 0 (K2 = 0 is moe_gemm_bf16); a2 may be
+ * NULL when K2 == 0. The composed block's output GEMM reads the routed
+ * experts' latent output and the shared experts' h this way, without copying
+ * them side by side. */
+moe_status moe_gemm_bf16_cat(const uint16_t* a1, int32_t K1, const uint16_t* a2, int32_t K2,
+                             const uint16_t* b, int64_t M, int32_t N, int32_t epilogue, void* c,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---- The composed latent-MoE block -----------------------------------------
+ * "Kimi K3.1 Pro at a glance": 896 routed experts (top-16, sigmoid routing)
+ * plus two shared experts; the routed experts work in a 3,584-wide latent,
+ * half the 7,168-wide hidden size; shared experts, latent up/down projections
+ * and router are BF16. "The MXFP4 latent MoE on FlyDSL": the two shared
+ * experts run on a second stream, concurrently with the routed experts. "Day
+ * 0 Kimi-K3 ...", "Kimi-K3 Architecture and Weights": Stable LatentMoE first
+ * projects the hidden state down to the latent.
+ *
+ * For hidden states h bf16 [T][hidden]:
+ *   x      = bf16(h . w_down^T)                      [T][d]     latent down
+ *   logits = h . w_router^T (fp32)                    [T][E]     router
+ *   y_lat  = moe_forward(x, logits)                   [T][d]     routed experts
+ *   hs     = bf16(silu(h . G^T) * (h . U^T))          [T][shared_I]
+ *   out    = bf16([y_lat | hs] . w_out^T)             [T][hidden]
+ * (fp32 accumulation in every product). Readings where the pages are silent:
+ * the router reads the hidden state; each shared expert is a SwiGLU MLP
+ * hidden -> 3,072 -> hidden, and the two are stored as one gated MLP of
+ * intermediate width shared_I = 6,144 (the sum of two gated MLPs is one gated
+ * MLP over their concatenated intermediate rows); the block's output is the
+ * latent up projection of y_lat plus the shared experts' output. */
+typedef struct {
+  int32_t T;        /* tokens */
+  int32_t hidden;   /* hidden width (7168); % 64 */
+  int32_t d;        /* latent width (3584) */
+  int32_t E;        /* routed experts (896); % 8 */
+  int32_t k;        /* experts per token (16) */
+  int32_t I;        /* routed expert intermediate width (3072) */
+  int32_t shared_I; /* intermediate width of all shared experts together (2 x 3072); % 128 */
+} moe_block_dims;
+
+typedef struct {
+  const uint16_t* w_down;     /* bf16 [d][hidden] latent down projection */
+  const uint16_t* w_router;   /* bf16 [E][hidden] */
+  const uint16_t* w_shared13; /* bf16 [2*shared_I][hidden]: the shared experts' gate rows
+                                 (expert 0 then expert 1), then their up rows, same order */
+  const uint16_t* w_out;      /* bf16 [hidden][d + shared_I]: columns 0..d-1 the latent up
+                                 projection, columns d.. the shared experts' down
+                                 projections (expert 0 then expert 1) */
+  moe_weights routed;         /* the routed experts, as for moe_forward */
+} moe_block_weights;
+
+/* Workspace bytes of moe_block_forward for these dims. The routed-layer
+ * shape rules of moe_workspace_size apply, plus hidden % 64 == 0, E % 8 == 0
+ * and shared_I % 128 == 0 (MOE_ERR_UNSUPPORTED otherwise). */
+moe_status moe_block_workspace_size(const moe_block_dims* dims, size_t* bytes);
+
+/* The block on `stream`, with the shared experts on `shared_stream`
+ * concurrently with the latent down projection, the router and the routed
+ * experts (fork and join by CUDA events; with shared_stream == stream
+ * everything runs in order on `stream`). Work that precedes the call on
+ * `stream` is complete before either stream reads h; when the call returns
+ * to the host, all its work is enqueued on `stream` (the join), so later
+ * work on `stream` sees `out`. kernel: the routed experts' GEMM family as in
+ * moe_forward. h, out 16-byte aligned; ws moe_block_workspace_size bytes,
+ * 256-byte aligned, status word at its start (moe_check_device_status);
+ * weights 16-byte aligned (routed weights as moe_forward). The fork and join
+ * events are created on the first call in each host thread for each device
+ * and kept; make that first call before any stream capture. Concurrent calls
+ * need distinct workspaces. */
+moe_status moe_block_forward(const moe_block_dims* dims, int32_t kernel, const uint16_t* h,
+                             const moe_block_weights* weights, uint16_t* out, void* ws,
+                             size_t ws_bytes, cudaStream_t stream, cudaStream_t shared_stream);
+
 /* Synchronises `stream`, then returns the status recorded in the workspace's
  * status word (MOE_OK if none). */
 moe_status moe_check_device_status(const void* ws, cudaStream_t stream);

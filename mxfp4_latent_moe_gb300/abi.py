@@ -40,6 +40,16 @@ class _Weights(ctypes.Structure):
     _fields_ = [("w13", _vp), ("w13_sf", _vp), ("w2", _vp), ("w2_sf", _vp)]
 
 
+class _BlockDims(ctypes.Structure):
+    _fields_ = [("T", _i32), ("hidden", _i32), ("d", _i32), ("E", _i32), ("k", _i32),
+                ("I", _i32), ("shared_I", _i32)]
+
+
+class _BlockWeights(ctypes.Structure):
+    _fields_ = [("w_down", _vp), ("w_router", _vp), ("w_shared13", _vp), ("w_out", _vp),
+                ("routed", _Weights)]
+
+
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_i32]),
     "moe_abi_version": (_i32, []),
@@ -70,6 +80,11 @@ _SIGS = {
     "moe_gemm_bf16": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "moe_router_logits": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "moe_gemm_bf16_workspace_size": (_sz, [_i64, _i32, _i32, _i32]),
+    "moe_gemm_bf16_cat": (_i32, [_vp, _i32, _vp, _i32, _vp, _i64, _i32, _i32, _vp, _vp, _sz,
+                                 _vp]),
+    "moe_block_workspace_size": (_i32, [ctypes.POINTER(_BlockDims), ctypes.POINTER(_sz)]),
+    "moe_block_forward": (_i32, [ctypes.POINTER(_BlockDims), _i32, _vp,
+                                 ctypes.POINTER(_BlockWeights), _vp, _vp, _sz, _vp, _vp]),
     "moe_check_device_status": (_i32, [_vp, _vp]),
     "moe_clear_device_status": (_i32, [_vp, _vp]),
     "moe_selftest_wait_timeout": (_i32, [_vp, _sz, ctypes.c_uint32, _vp]),
@@ -253,6 +268,31 @@ def moe_gemm_bf16_workspace_size(M, N, K, epilogue):
 def moe_router_logits(x, w_router, T, d_in, E, logits, ws, stream=None):
     _call("moe_router_logits", _ptr(x), _ptr(w_router), T, d_in, E, _ptr(logits), _ptr(ws),
           ws.numel() * ws.element_size(), _stream(stream))
+
+
+def moe_gemm_bf16_cat(a1, K1, a2, K2, b, M, N, epilogue, c, ws, stream=None):
+    """C = [A1 | A2] . B^T: a1 bf16 [M][K1], a2 bf16 [M][K2], b [N][K1 + K2]."""
+    _call("moe_gemm_bf16_cat", _ptr(a1), K1, _ptr(a2), K2, _ptr(b), M, N, epilogue, _ptr(c),
+          _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+
+
+def moe_block_workspace_size(T, hidden, d, E, k, I, shared_I):
+    n = _sz(0)
+    _call("moe_block_workspace_size", ctypes.byref(_BlockDims(T, hidden, d, E, k, I, shared_I)),
+          ctypes.byref(n))
+    return n.value
+
+
+def moe_block_forward(T, hidden, d, E, k, I, shared_I, kernel, h, w_down, w_router, w_shared13,
+                      w_out, w13, w13_sf, w2, w2_sf, out, ws, stream=None, shared_stream=None):
+    """The composed block; shared_stream None runs everything on `stream`."""
+    W = _BlockWeights(_ptr(w_down), _ptr(w_router), _ptr(w_shared13), _ptr(w_out),
+                      _Weights(_ptr(w13), _ptr(w13_sf), _ptr(w2), _ptr(w2_sf)))
+    st = _stream(stream)
+    side = st if shared_stream is None else _stream(shared_stream)
+    _call("moe_block_forward", ctypes.byref(_BlockDims(T, hidden, d, E, k, I, shared_I)), kernel,
+          _ptr(h), ctypes.byref(W), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), st,
+          side)
 
 
 def moe_check_device_status(ws, stream=None):

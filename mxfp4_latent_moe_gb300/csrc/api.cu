@@ -360,6 +360,29 @@ moe_status moe_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int32_
                                          static_cast<int*>(ws), stream));
 }
 
+moe_status moe_gemm_bf16_cat(const uint16_t* a1, int32_t K1, const uint16_t* a2, int32_t K2,
+                             const uint16_t* b, int64_t M, int32_t N, int32_t epilogue, void* c,
+                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (M < 0 || N < 0 || K1 < 0 || K2 < 0) return MOE_ERR_INVALID_ARGUMENT;
+  if (epilogue != MOE_EPI_F32 && epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_BF16)
+    return MOE_ERR_UNSUPPORTED;
+  const int64_t K = int64_t(K1) + K2;
+  if (K1 < 64 || K1 % 64 != 0 || K2 % 64 != 0 || K > (1 << 20) || N < 8 || N % 8 != 0 ||
+      N > (1 << 20) || M >= int64_t(INT32_MAX))
+    return MOE_ERR_UNSUPPORTED;
+  if (epilogue == MOE_EPI_SWIGLU_BF16 && N % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  if (M == 0) return MOE_OK;
+  if (!a1 || (K2 > 0 && !a2) || !b || !c || !ws) return MOE_ERR_INVALID_ARGUMENT;
+  if (!aligned(a1, 16) || (K2 > 0 && !aligned(a2, 16)) || !aligned(b, 16) || !aligned(c, 16) ||
+      !aligned(ws, 16))
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < MOE_STATUS_BYTES + moe::bf16_partial_bytes(M, N, int(K), epilogue))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(moe::launch_gemm_bf16_cat(a1, K1, a2, K2, b, M, N, epilogue, c,
+                                             at<float>(ws, MOE_STATUS_BYTES),
+                                             static_cast<int*>(ws), stream));
+}
+
 size_t moe_gemm_bf16_workspace_size(int64_t M, int32_t N, int32_t K, int32_t epilogue) {
   if (M < 0 || N < 8 || N % 8 != 0 || K < 64 || K % 64 != 0) return 0;
   if (epilogue != MOE_EPI_F32 && epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_BF16)
@@ -410,11 +433,13 @@ namespace {
 
 // The layer, MXFP8 (a4w4 = false) or with MXFP4 stage-1 activations. kernel
 // is the GEMM family of both stages (MXFP8) or of stage 2 (A4W4, whose stage 1
-// always runs on token tiles).
+// always runs on token tiles). Device problems go to `status_out` when given
+// (the composed block's status word, already cleared by the caller), else to
+// the status word at the start of ws, which this call clears first.
 moe_status forward_impl(bool a4w4, const moe_dims* dims, int32_t kernel, const uint16_t* x,
                         const float* logits, const moe_weights* W, uint16_t* y,
                         int32_t* topk_ids_out, float* topk_w_out, void* ws, size_t ws_bytes,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int* status_out = nullptr) {
   moe_status s = check_dims(dims);
   if (s != MOE_OK) return s;
   if (a4w4 && dims->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
@@ -433,8 +458,8 @@ moe_status forward_impl(bool a4w4, const moe_dims* dims, int32_t kernel, const u
   const ForwardLayout L = a4w4 ? forward_layout_a4w4(D, kernel) : forward_layout(D, kernel);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
 
-  int* status = at<int>(ws, L.status);
-  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), stream);
+  int* status = status_out ? status_out : at<int>(ws, L.status);
+  cudaError_t e = status_out ? cudaSuccess : cudaMemsetAsync(status, 0, sizeof(int), stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (D.k == 0) return from_cuda(cudaMemsetAsync(y, 0, size_t(D.T) * D.d * 2, stream));
 
@@ -513,6 +538,22 @@ moe_status moe_forward_a4w4(const moe_dims* dims, int32_t kernel, const uint16_t
   return forward_impl(true, dims, kernel, x, logits, W, y, topk_ids_out, topk_w_out, ws,
                       ws_bytes, stream);
 }
+
+}  // extern "C"
+
+namespace moe {
+
+moe_status forward_with_status(bool a4w4, const moe_dims* dims, int32_t kernel,
+                               const uint16_t* x, const float* logits, const moe_weights* W,
+                               uint16_t* y, void* ws, size_t ws_bytes, int* status,
+                               cudaStream_t stream) {
+  return forward_impl(a4w4, dims, kernel, x, logits, W, y, nullptr, nullptr, ws, ws_bytes, stream,
+                      status);
+}
+
+}  // namespace moe
+
+extern "C" {
 
 moe_status moe_check_device_status(const void* ws, cudaStream_t stream) {
   if (!ws || !aligned(ws, 4)) return MOE_ERR_INVALID_ARGUMENT;

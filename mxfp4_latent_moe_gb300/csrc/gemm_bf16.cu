@@ -20,6 +20,9 @@
 // run in groups of 8 row tiles with the row tile fastest, so the CTAs in
 // flight share B tiles and keep a bounded slice of A in L2. Rows of A and B
 // past M and N are zero-filled by TMA; stores past M and N are skipped.
+// A may come in two parts along K, A = [A1 | A2] (A1 [M][K1], A2 [M][K2],
+// two tensor maps): the composed block's output GEMM reads the routed
+// experts' latent output and the shared experts' h side by side this way.
 // Calls with too few tiles to cover the GPU (decode: one row tile) split K:
 // each CTA accumulates one K-slice of a tile and writes its fp32 partial sums
 // to the workspace; a second kernel adds the slices in a fixed order and
@@ -73,6 +76,7 @@ struct Bf16Params {
   int64_t M;
   int N;          // rows of B
   int K;
+  int K1T;        // stages whose A columns come from the first A map (the rest: the second)
   int MT, NT;     // row tiles of A; column tiles of C (EPI kEpiSwiglu: of h)
   int KS;         // K-slices per tile (1: no split)
   int KTS;        // 64-input stages per slice
@@ -99,6 +103,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                     const __grid_constant__ CUtensorMap tmap_a2,
                      const __grid_constant__ CUtensorMap tmap_b, const Bf16Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -158,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + kOffA + stage * A_BYTES;
           uint8_t* sb = smem + kOffB + stage * B_BYTES;
           mbar_arrive_expect_tx(&full[stage], kStageTx);
-          tma_load_2d(sa, &tmap_a, &full[stage], kt * BKB, mt * BM);
+          // A = [A1 | A2] along K: stages below K1T read A1, the rest A2
+          if (kt < p.K1T) tma_load_2d(sa, &tmap_a, &full[stage], kt * BKB, mt * BM);
+          else tma_load_2d(sa, &tmap_a2, &full[stage], (kt - p.K1T) * BKB, mt * BM);
           if (EPI == kEpiSwiglu) {   // 128 gate rows, then the matching 128 up rows
             tma_load_2d(sb, &tmap_b, &full[stage], kt * BKB, nt * 128);
             tma_load_2d(sb + B_BYTES / 2, &tmap_b, &full[stage], kt * BKB,
@@ -397,14 +404,14 @@ bool encode_bf16(CUtensorMap* map, const void* base, int K, int64_t rows, int bo
 }
 
 template <int EPI>
-cudaError_t launch_epi_main(const Bf16Params& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                            cudaStream_t st);
+cudaError_t launch_epi_main(const Bf16Params& p, const CUtensorMap& ta, const CUtensorMap& ta2,
+                            const CUtensorMap& tb, cudaStream_t st);
 
 template <int EPI>
-cudaError_t launch_epi(const Bf16Params& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                       cudaStream_t st) {
+cudaError_t launch_epi(const Bf16Params& p, const CUtensorMap& ta, const CUtensorMap& ta2,
+                       const CUtensorMap& tb, cudaStream_t st) {
   if (p.KS > 1) {
-    cudaError_t err = launch_epi_main<EPI>(p, ta, tb, st);
+    cudaError_t err = launch_epi_main<EPI>(p, ta, ta2, tb, st);
     if (err != cudaSuccess) return err;
     const int n_out = EPI == kEpiSwiglu ? (p.N >> 1) : p.N;
     const int64_t groups = p.M * (n_out / 4);
@@ -412,12 +419,12 @@ cudaError_t launch_epi(const Bf16Params& p, const CUtensorMap& ta, const CUtenso
                      dim3(256), 0, st, 1, static_cast<const float*>(p.partial), p.KS, p.M, p.N,
                      p.c);
   }
-  return launch_epi_main<EPI>(p, ta, tb, st);
+  return launch_epi_main<EPI>(p, ta, ta2, tb, st);
 }
 
 template <int EPI>
-cudaError_t launch_epi_main(const Bf16Params& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                            cudaStream_t st) {
+cudaError_t launch_epi_main(const Bf16Params& p, const CUtensorMap& ta, const CUtensorMap& ta2,
+                            const CUtensorMap& tb, cudaStream_t st) {
   cudaError_t err = cudaFuncSetAttribute(gemm_bf16_kernel<EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
@@ -427,7 +434,7 @@ cudaError_t launch_epi_main(const Bf16Params& p, const CUtensorMap& ta, const CU
   const int64_t work = int64_t(p.MT) * p.NT * p.KS;
   const int grid = int(work < sms ? work : sms);
   return launch_ex(true, gemm_bf16_kernel<EPI>, dim3(grid), dim3(kThreads), kSmemBytes, st, 1, ta,
-                   tb, p);
+                   ta2, tb, p);
 }
 
 }  // namespace
@@ -454,16 +461,24 @@ size_t bf16_partial_bytes(int64_t M, int N, int K, int epilogue) {
   return ks > 1 ? size_t(ks) * size_t(M) * size_t(N) * 4 : 0;
 }
 
-cudaError_t launch_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int N, int K,
-                             int epilogue, void* c, float* partial, int* status, cudaStream_t st) {
+cudaError_t launch_gemm_bf16_cat(const uint16_t* a1, int K1, const uint16_t* a2, int K2,
+                                 const uint16_t* b, int64_t M, int N, int epilogue, void* c,
+                                 float* partial, int* status, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
-  CUtensorMap ta, tb;
-  if (!encode_bf16(&ta, a, K, M, BM)) return cudaErrorInvalidValue;
+  const int K = K1 + K2;
+  CUtensorMap ta, ta2, tb;
+  if (!encode_bf16(&ta, a1, K1, M, BM)) return cudaErrorInvalidValue;
+  if (K2 > 0) {
+    if (!encode_bf16(&ta2, a2, K2, M, BM)) return cudaErrorInvalidValue;
+  } else {
+    ta2 = ta;   // never read: every stage is below K1T
+  }
   if (!encode_bf16(&tb, b, K, N, epilogue == kEpiSwiglu ? 128 : BN)) return cudaErrorInvalidValue;
   Bf16Params p{};
   p.M = M;
   p.N = N;
   p.K = K;
+  p.K1T = K1 / BKB;
   p.MT = int((M + BM - 1) / BM);
   p.NT = epilogue == kEpiSwiglu ? (N / 2) / 128 : (N + BN - 1) / BN;
   p.KS = bf16_k_splits(M, N, K, epilogue);
@@ -471,9 +486,14 @@ cudaError_t launch_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, in
   p.partial = partial;
   p.c = c;
   p.status = status;
-  if (epilogue == kEpiF32) return launch_epi<kEpiF32>(p, ta, tb, st);
-  if (epilogue == kEpiBf16) return launch_epi<kEpiBf16>(p, ta, tb, st);
-  return launch_epi<kEpiSwiglu>(p, ta, tb, st);
+  if (epilogue == kEpiF32) return launch_epi<kEpiF32>(p, ta, ta2, tb, st);
+  if (epilogue == kEpiBf16) return launch_epi<kEpiBf16>(p, ta, ta2, tb, st);
+  return launch_epi<kEpiSwiglu>(p, ta, ta2, tb, st);
+}
+
+cudaError_t launch_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int N, int K,
+                             int epilogue, void* c, float* partial, int* status, cudaStream_t st) {
+  return launch_gemm_bf16_cat(a, K, nullptr, 0, b, M, N, epilogue, c, partial, status, st);
 }
 
 }  // namespace moe

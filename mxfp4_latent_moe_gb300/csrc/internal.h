@@ -86,7 +86,19 @@ int bf16_k_splits(int64_t M, int N, int K, int epilogue);
 size_t bf16_partial_bytes(int64_t M, int N, int K, int epilogue);   // 0 without a split
 cudaError_t launch_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int N, int K,
                              int epilogue, void* c, float* partial, int* status, cudaStream_t st);
+// The same with A = [A1 | A2] along K (A1 [M][K1], A2 [M][K2], K1 and K2
+// multiples of 64; K2 may be 0): C = A1 . B[:, :K1]^T + A2 . B[:, K1:]^T.
+cudaError_t launch_gemm_bf16_cat(const uint16_t* a1, int K1, const uint16_t* a2, int K2,
+                                 const uint16_t* b, int64_t M, int N, int epilogue, void* c,
+                                 float* partial, int* status, cudaStream_t st);
 cudaError_t launch_wait_timeout_selftest(int* status, uint32_t limit_us, cudaStream_t st);
+
+// moe_forward / moe_forward_a4w4 with device problems recorded in `status`
+// (not cleared here) instead of the workspace's own status word.
+moe_status forward_with_status(bool a4w4, const moe_dims* dims, int32_t kernel,
+                               const uint16_t* x, const float* logits, const moe_weights* W,
+                               uint16_t* y, void* ws, size_t ws_bytes, int* status,
+                               cudaStream_t stream);
 
 cudaError_t launch_combine(const uint16_t* yp, const int* slot_to_row, const float* w, int T,
                            int k, int d, uint16_t* y, cudaStream_t st);

@@ -81,6 +81,50 @@ class MoeLayer:
         return g, y, ws
 
 
+class MoeBlock:
+    """The composed latent-MoE block (moe_block_forward): latent down
+    projection and router on the hidden state, the routed experts in the
+    latent, the two shared experts beside them on a second stream, and one
+    output GEMM that adds the latent up projection of the routed output to the
+    shared experts' down projection.
+
+    BF16 weights (CUDA tensors): w_down [d][hidden], w_router [E][hidden],
+    w_shared13 [2*shared_I][hidden] (both shared experts' gate rows, then
+    their up rows), w_out [hidden][d + shared_I] (latent up columns, then the
+    shared experts' down columns). Routed weights as MoeLayer.
+    """
+
+    def __init__(self, w_down, w_router, w_shared13, w_out, w13, w13_s, w2, w2_s, k,
+                 kernel=abi.GEMM_AUTO):
+        self.layer = MoeLayer(w13, w13_s, w2, w2_s, k, kernel=kernel)
+        self.w_down, self.w_router = w_down.contiguous(), w_router.contiguous()
+        self.w_shared13, self.w_out = w_shared13.contiguous(), w_out.contiguous()
+        self.hidden = w_down.shape[1]
+        self.shared_I = w_shared13.shape[0] // 2
+
+    def dims(self, T):
+        L = self.layer
+        return (T, self.hidden, L.d, L.E, L.k, L.I, self.shared_I)
+
+    def workspace(self, T):
+        n = abi.moe_block_workspace_size(*self.dims(T))
+        return torch.empty(n, dtype=torch.uint8, device=self.w_down.device)
+
+    def forward(self, h, ws=None, out=None, stream=None, shared_stream=None):
+        """out = the block on hidden states h bf16 [T][hidden]. shared_stream:
+        the stream the shared experts run on (None: everything on `stream`)."""
+        T = h.shape[0]
+        if ws is None:
+            ws = self.workspace(T)
+        if out is None:
+            out = torch.empty(T, self.hidden, dtype=torch.bfloat16, device=h.device)
+        L = self.layer
+        abi.moe_block_forward(*self.dims(T), L.kernel_for(T), h, self.w_down, self.w_router,
+                              self.w_shared13, self.w_out, L.w13, L.w13_sf, L.w2, L.w2_sf, out,
+                              ws, stream=stream, shared_stream=shared_stream)
+        return out
+
+
 class HostPipeline:
     """Runs the layer on batches held in (pinned) host memory with the copies
     off the compute stream.

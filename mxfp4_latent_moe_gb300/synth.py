@@ -125,6 +125,73 @@ def make_layer(wl: Workload, seed=0, device="cpu"):
     return dict(x=x, logits=logits, **weights)
 
 
+@dataclass(frozen=True)
+class BlockWorkload:
+    """The composed block around the routed layer: hidden width, latent d,
+    routed experts (E, k, I) and the shared experts' total intermediate width
+    ("Kimi K3.1 Pro at a glance": hidden 7,168, latent 3,584, two shared
+    experts; each shared expert 7,168 -> 3,072 -> 7,168)."""
+    name: str
+    T: int
+    hidden: int
+    d: int
+    E: int
+    k: int
+    I: int
+    shared_I: int
+
+    @property
+    def routed(self):
+        return Workload(self.name + "_routed", T=self.T, d=self.d, E=self.E, k=self.k, I=self.I)
+
+
+BLOCK_WORKLOADS = [
+    BlockWorkload("block_decode_t64", T=64, hidden=7168, d=3584, E=896, k=16, I=3072,
+                  shared_I=6144),
+    BlockWorkload("block_prefill_t8192", T=8192, hidden=7168, d=3584, E=896, k=16, I=3072,
+                  shared_I=6144),
+]
+BLOCK_BY_NAME = {w.name: w for w in BLOCK_WORKLOADS}
+
+
+def block_workload(name):
+    return BLOCK_BY_NAME[name]
+
+
+def block_shape(name, T, hidden, d, E, k, I, shared_I):
+    return BlockWorkload(name, T=T, hidden=hidden, d=d, E=E, k=k, I=I, shared_I=shared_I)
+
+
+def _grid_bf16(shape_, scale, lo, hi, g, device):
+    """Integers uniform in [lo, hi] times `scale` (a power of two), as bf16."""
+    v = torch.randint(lo, hi + 1, shape_, generator=g, device=device, dtype=torch.int32)
+    return (v.to(torch.float32) * scale).to(torch.bfloat16)
+
+
+def make_block(bw: BlockWorkload, seed=0, device="cpu"):
+    """All inputs of one block call. Draw order: h, w_down, w_router,
+    w_shared13, w_out, then the routed experts' weights (as make_weights).
+
+    Values sit on coarse power-of-two grids so that every product the block's
+    BF16 GEMMs form before a rounding is exact in fp32: h = N(0,1) rounded to
+    multiples of 1/8 and clamped to [-4, 4]; every BF16 weight an integer
+    uniform in [-16, 16] times 2^-8. A dot product over 7,168 inputs is then a
+    multiple of 2^-11 below 2^11 in magnitude (22 significant bits), so the
+    router logits and the latent x are the same whatever the order of the
+    fp32 additions: the routing decisions that depend on them cannot differ
+    between two correct implementations."""
+    g = _gen(seed, device)
+    T, hd, d, E, Is = bw.T, bw.hidden, bw.d, bw.E, bw.shared_I
+    h = (torch.randn(T, hd, generator=g, device=device) * 8).round().clamp(-32, 32) / 8
+    out = dict(h=h.to(torch.bfloat16))
+    out["w_down"] = _grid_bf16((d, hd), 2.0 ** -8, -16, 16, g, device)
+    out["w_router"] = _grid_bf16((E, hd), 2.0 ** -8, -16, 16, g, device)
+    out["w_shared13"] = _grid_bf16((2 * Is, hd), 2.0 ** -8, -16, 16, g, device)
+    out["w_out"] = _grid_bf16((hd, d + Is), 2.0 ** -8, -16, 16, g, device)
+    out.update(make_weights(bw.routed, g=g, device=device))
+    return out
+
+
 def random_e4m3_codes(shape_, seed=0, device="cpu", g=None):
     """Uniform finite E4M3 codes (magnitude codes 0x00..0x7E, either sign)."""
     g = g if g is not None else _gen(seed, device)

@@ -49,6 +49,7 @@ def lib():
             "orc_expert_bytes": (_i64, [_i32, _i32]),
             "orc_e2m1_encode_rne_sat": (ctypes.c_uint8, [ctypes.c_double]),
             "orc_gemm_bf16": (None, [_u16p, _u16p, _i64, _i64, _i64, _f64p]),
+            "orc_bf16_rne_n": (None, [_f64p, _i64, _u16p]),
             "orc_gemm_bf16_swiglu": (None, [_u16p, _u16p, _i64, _i64, _i64, _f64p]),
             "orc_mxfp4_quant_block": (None, [_f32p, _u8p, _u8p]),
             "orc_mxfp4_quant_rows": (None, [_f32p, _i64, _i64, _u8p, _u8p]),
@@ -225,24 +226,89 @@ def moe_forward(x_bits, logits, k, w13, w13s, w2, w2s, threads=0, want_y64=False
     return dict(y=y, ids=ids[:, :k], w=w[:, :k], y64=y64)
 
 
-def gemm_bf16(a_bits, b_bits):
+def _by_rows(fn, a, n_out, threads):
+    """fn(a_rows, out_rows) over row chunks of a on `threads` host threads
+    (0 = all cores; the rows are independent and the library call releases
+    the interpreter lock)."""
+    import concurrent.futures as cf
+    M = a.shape[0]
+    out = np.empty((M, n_out), np.float64)
+    n = threads if threads > 0 else (os.cpu_count() or 1)
+    n = max(1, min(n, M))
+    if n == 1:
+        fn(a, out)
+        return out
+    parts = [p for p in np.array_split(np.arange(M), n) if len(p)]
+
+    def run(p):
+        o = np.empty((len(p), n_out), np.float64)
+        fn(np.ascontiguousarray(a[p[0]:p[-1] + 1]), o)
+        out[p[0]:p[-1] + 1] = o
+
+    with cf.ThreadPoolExecutor(len(parts)) as ex:
+        list(ex.map(run, parts))
+    return out
+
+
+def gemm_bf16(a_bits, b_bits, threads=1):
     """C = A . B^T in fp64; a_bits [M][K], b_bits [N][K] bf16 bit patterns."""
     a, b = _c(a_bits, np.uint16), _c(b_bits, np.uint16)
-    M, K = a.shape
+    K = a.shape[1]
     N = b.shape[0]
-    c = np.empty((M, N), np.float64)
-    lib().orc_gemm_bf16(_p(a, _u16p), _p(b, _u16p), M, N, K, _p(c, _f64p))
-    return c
+
+    def fn(ar, c):
+        lib().orc_gemm_bf16(_p(ar, _u16p), _p(b, _u16p), ar.shape[0], N, K, _p(c, _f64p))
+    return _by_rows(fn, a, N, threads)
 
 
-def gemm_bf16_swiglu(a_bits, b_bits):
+def gemm_bf16_swiglu(a_bits, b_bits, threads=1):
     """h = silu(A . Bgate^T) * (A . Bup^T) in fp64; b_bits [2*Nh][K], gate rows first."""
     a, b = _c(a_bits, np.uint16), _c(b_bits, np.uint16)
-    M, K = a.shape
+    K = a.shape[1]
     Nh = b.shape[0] // 2
-    h = np.empty((M, Nh), np.float64)
-    lib().orc_gemm_bf16_swiglu(_p(a, _u16p), _p(b, _u16p), M, Nh, K, _p(h, _f64p))
-    return h
+
+    def fn(ar, h):
+        lib().orc_gemm_bf16_swiglu(_p(ar, _u16p), _p(b, _u16p), ar.shape[0], Nh, K, _p(h, _f64p))
+    return _by_rows(fn, a, Nh, threads)
+
+
+def bf16_rne_array(v):
+    """fp64 array -> bf16 bit patterns (uint16), round to nearest even."""
+    v = _c(v, np.float64)
+    out = np.empty(v.shape, np.uint16)
+    lib().orc_bf16_rne_n(_p(v, _f64p), v.size, _p(out, _u16p))
+    return out
+
+
+def block_forward(h_bits, k, w_down, w_router, w_shared13, w_out, w13, w13s, w2, w2s,
+                  threads=0):
+    """The composed latent-MoE block, step by step from the functions above
+    ("Kimi K3.1 Pro at a glance": routed experts in a latent half the hidden
+    width, two shared experts, BF16 router and latent projections; "Day 0
+    Kimi-K3 ...", "Kimi-K3 Architecture and Weights": the hidden state is
+    projected down to the latent before the experts). Every tensor that passes
+    between steps is held in the format the library passes it in: x, the
+    routed output and the shared experts' h as bf16, the logits as fp32.
+
+      x      = bf16(h . w_down^T)                 [T][d]
+      logits = fp32(h . w_router^T)               [T][E]
+      y_lat  = moe_forward(x, logits)             [T][d] (bf16)
+      hs     = bf16(silu(h . G^T) * (h . U^T))    [T][shared_I]
+      out    = bf16([y_lat | hs] . w_out^T)       [T][hidden]
+
+    h_bits bf16 patterns [T][hidden]; bf16 weights as bit patterns: w_down
+    [d][hidden], w_router [E][hidden], w_shared13 [2 shared_I][hidden] (gate
+    rows then up rows), w_out [hidden][d + shared_I]; routed weights as
+    moe_forward. Returns dict(y (bf16 bits), y64 (fp64 before the last
+    rounding), x, logits, ids, w, y_lat, hs)."""
+    h = _c(h_bits, np.uint16)
+    x = bf16_rne_array(gemm_bf16(h, w_down, threads))
+    logits = gemm_bf16(h, w_router, threads).astype(np.float32)
+    routed = moe_forward(x, logits, k, w13, w13s, w2, w2s, threads=threads)
+    hs = bf16_rne_array(gemm_bf16_swiglu(h, w_shared13, threads))
+    y64 = gemm_bf16(np.concatenate([routed["y"], hs], axis=1), w_out, threads)
+    return dict(y=bf16_rne_array(y64), y64=y64, x=x, logits=logits, ids=routed["ids"],
+                w=routed["w"], y_lat=routed["y"], hs=hs)
 
 
 def expert_bytes(d, I):

@@ -435,6 +435,10 @@ void orc_gemm_bf16_swiglu(const uint16_t* a, const uint16_t* b, int64_t M, int64
   }
 }
 
+void orc_bf16_rne_n(const double* v, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_rne(v[i]);
+}
+
 int64_t orc_expert_bytes(int32_t d, int32_t I) {
   // Three I x d matrices: d*I/2 bytes of packed E2M1 and d*I/32 scale bytes each.
   return int64_t(3) * (int64_t(d) * I / 2 + int64_t(d) * I / 32);

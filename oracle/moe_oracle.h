@@ -158,6 +158,9 @@ void orc_gemm_bf16_swiglu(const uint16_t* a, const uint16_t* b, int64_t M, int64
 /* Round a real number to the nearest bf16 (ties to even), returning its bits. */
 uint16_t orc_bf16_rne(double v);
 
+/* orc_bf16_rne over n values (a block's bf16 intermediates and output). */
+void orc_bf16_rne_n(const double* v, int64_t n, uint16_t* out);
+
 /* The whole layer for n independent tokens.
  * x [n][d] bf16 bits, logits [n][E] fp32, weights for all E experts:
  * w13 [E][2I][d/2], w13s [E][2I][d/32], w2 [E][d][I/2], w2s [E][d][I/32].

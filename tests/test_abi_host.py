@@ -157,3 +157,29 @@ def test_host_validation_rejects_before_any_launch(L):
     # status helpers
     assert _rc(L, "moe_check_device_status", None, None) == abi.INVALID_ARGUMENT
     assert _rc(L, "moe_selftest_wait_timeout", fake, 8, 100, None) == abi.WORKSPACE_TOO_SMALL
+
+
+def test_block_sizes_and_host_validation(L):
+    full = (64, 7168, 3584, 896, 16, 3072, 6144)
+    n = abi.moe_block_workspace_size(*full)
+    layer = abi.moe_workspace_size(64, 3584, 896, 16, 3072)
+    # status + x + logits + routed output + shared h + two GEMM workspaces + the layer's
+    assert n >= layer + 64 * (3584 * 2 * 2 + 896 * 4 + 6144 * 2)
+    for bad, code in (((64, 7168, 3584, 900, 16, 3072, 6144), abi.UNSUPPORTED),   # E % 8
+                      ((64, 7100, 3584, 896, 16, 3072, 6144), abi.UNSUPPORTED),   # hidden % 64
+                      ((64, 7168, 3584, 896, 16, 3072, 6000), abi.UNSUPPORTED),   # shared_I % 128
+                      ((64, 7168, 3500, 896, 16, 3072, 6144), abi.UNSUPPORTED),   # d % 128
+                      ((-1, 7168, 3584, 896, 16, 3072, 6144), abi.INVALID_ARGUMENT)):
+        with pytest.raises(abi.MoeError) as err:
+            abi.moe_block_workspace_size(*bad)
+        assert err.value.code == code
+    # null pointers are refused on the host, before any launch
+    dims = abi._BlockDims(*full)
+    W = abi._BlockWeights(None, None, None, None, abi._Weights(None, None, None, None))
+    rc = L.moe_block_forward(ctypes.byref(dims), 0, None, ctypes.byref(W), None, None, 0, None,
+                             None)
+    assert rc == abi.INVALID_ARGUMENT
+    rc = L.moe_gemm_bf16_cat(None, 64, None, 64, None, 8, 8, 1, None, None, 0, None)
+    assert rc == abi.INVALID_ARGUMENT
+    rc = L.moe_gemm_bf16_cat(None, 32, None, 64, None, 8, 8, 1, None, None, 0, None)
+    assert rc == abi.UNSUPPORTED    # K1 below one 64-input stage

@@ -13,6 +13,7 @@ import pytest
 import torch
 from scipy.special import expit
 
+from mxfp4_latent_moe_gb300 import synth
 from tests import gpu_util as gu
 from tests import mx_numpy as mx
 
@@ -82,19 +83,25 @@ def test_gemm_bf16_swiglu_matches_oracle(abi, orc, M, Nh, K):
 
 @pytest.mark.parametrize("T", [64, 512])
 def test_router_logits_feed_the_routing(abi, orc, T):
+    """The router at the layer's sizes on the composed block's power-of-two
+    input grid, where every fp32 sum is exact: the GPU logits equal the
+    oracle's bit for bit, and routing them on the GPU gives the oracle's
+    routing of its own logits."""
     d_in, E, k = 7168, 896, 16
-    x, w = _operands(T, E, d_in, seed=T, scale_b=0.02)
+    B = synth.make_block(synth.block_shape("router", T=T, hidden=d_in, d=128, E=E, k=k, I=128,
+                                           shared_I=128), seed=T)
+    x, w = B["h"], B["w_router"]
     logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
     ws = torch.zeros(abi.moe_gemm_bf16_workspace_size(T, E, d_in, 0), dtype=torch.uint8,
                      device="cuda")
     abi.moe_router_logits(x.cuda(), w.cuda(), T, d_in, E, logits, ws)
     assert abi.moe_check_device_status(ws) == 0
-    ref = orc.gemm_bf16(_bits(x), _bits(w))
+    ref = orc.gemm_bf16(_bits(x), _bits(w), threads=0)
     got = logits.cpu().numpy().astype(np.float64)
-    assert np.all(np.abs(got - ref) <= 1e-5 * _absdot(x, w) + 1e-30)
-    # the routing of the GPU logits equals the oracle's routing of the same logits
+    assert np.array_equal(got, ref)
     ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
     wts = torch.empty(T, k, dtype=torch.float32, device="cuda")
     abi.moe_route_topk(logits, T, E, k, ids, wts)
-    rids, _ = orc.route_topk(logits.cpu().numpy(), k)
+    rids, rw = orc.route_topk(ref.astype(np.float32), k)
     assert np.array_equal(ids.cpu().numpy(), rids)
+    np.testing.assert_allclose(wts.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
