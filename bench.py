@@ -69,7 +69,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=0, help="oracle tokens (0 = automatic)")
-    ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "token", "weight"],
+    ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "token", "weight", "pair"],
                     help="grouped-GEMM family (auto = the library's default for the shape)")
     ap.add_argument("--step", default="", choices=["", "router", "latent_down", "latent_up",
                                                    "shared_experts", "block"],
@@ -163,6 +163,8 @@ FAMILY_SOURCES = {
     "token_tiles": ["mxfp4_latent_moe_gb300/csrc/gemm.cu", "mxfp4_latent_moe_gb300/csrc/common.cuh"],
     "weight_tiles": ["mxfp4_latent_moe_gb300/csrc/gemm_decode.cu",
                      "mxfp4_latent_moe_gb300/csrc/common.cuh"],
+    "pair_tiles": ["mxfp4_latent_moe_gb300/csrc/gemm_pair.cu",
+                   "mxfp4_latent_moe_gb300/csrc/common.cuh"],
 }
 
 
@@ -479,7 +481,7 @@ def measure_layer(args, wl, dev, sampler, a4w4=False):
 
     L = synth.make_layer(wl, seed=args.seed, device=dev)
     kernel_arg = {"auto": abi.GEMM_AUTO, "token": abi.GEMM_TOKEN_TILES,
-                  "weight": abi.GEMM_WEIGHT_TILES}[args.gemm_kernel]
+                  "weight": abi.GEMM_WEIGHT_TILES, "pair": abi.GEMM_PAIR_TILES}[args.gemm_kernel]
     layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k, kernel=kernel_arg)
     T, d, E, k, I = wl.T, wl.d, wl.E, wl.k, wl.I
     x, logits = L["x"], L["logits"]
@@ -612,7 +614,8 @@ def measure_layer(args, wl, dev, sampler, a4w4=False):
     bound = "hbm" if t_mem >= t_math else "tensor"
     ms_per_step = total_ms / args.steps
     layer_frac = max(t_mem, t_math) / (ms_per_step / 1e3)
-    family = "weight_tiles" if kernel == abi.GEMM_WEIGHT_TILES else "token_tiles"
+    family = {abi.GEMM_WEIGHT_TILES: "weight_tiles", abi.GEMM_PAIR_TILES: "pair_tiles"}.get(
+        kernel, "token_tiles")
     dom = "gemm_w13_glu"
     dom_s = kms[dom] / 1e3
     x_row_bytes = (d // 2 if a4w4 else d) + d // 32

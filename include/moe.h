@@ -53,6 +53,14 @@
  *                          a few tokens per expert (decode), where streaming
  *                          the weights from HBM is the bound. Groups padded to
  *                          32 rows; activation scales in the GROUP32 layout.
+ *   MOE_GEMM_PAIR_TILES    weights are the M side of an MMA spread over a pair
+ *                          of SMs (2-CTA clusters, 256 weight rows per MMA),
+ *                          an expert's tokens the N side in chunks of 128
+ *                          (stage 1) or 256 (stage 2), the last chunk as wide
+ *                          as its tokens rounded up to 16; for many tokens per
+ *                          expert (prefill). Groups padded to 128 rows;
+ *                          activation scales TILED (as token tiles). Needs
+ *                          d % 256 == 0 and I % 256 == 0.
  *
  * Data layouts:
  *   x, y        bf16 [T][d] row-major.
@@ -113,7 +121,8 @@ typedef enum {
 typedef enum {
   MOE_GEMM_AUTO = 0,         /* moe_forward only: see moe_default_kernel */
   MOE_GEMM_TOKEN_TILES = 1,  /* tokens on the MMA's M side */
-  MOE_GEMM_WEIGHT_TILES = 2  /* weights on the MMA's M side, tokens as N */
+  MOE_GEMM_WEIGHT_TILES = 2, /* weights on the MMA's M side, tokens as N */
+  MOE_GEMM_PAIR_TILES = 3    /* weights on M across a pair of SMs, tokens as N */
 } moe_gemm_kernel;
 
 typedef struct {

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 
 STATUS_BYTES = 256
 OK, INVALID_ARGUMENT, UNSUPPORTED, WORKSPACE_TOO_SMALL, CUDA, DEVICE_TIMEOUT, DEVICE_BAD_INPUT = range(7)
-GEMM_AUTO, GEMM_TOKEN_TILES, GEMM_WEIGHT_TILES = range(3)
+GEMM_AUTO, GEMM_TOKEN_TILES, GEMM_WEIGHT_TILES, GEMM_PAIR_TILES = range(4)
 SCALES_TILED128, SCALES_GROUP32 = range(2)
 EPI_F32, EPI_BF16, EPI_SWIGLU_BF16 = range(3)
 

@@ -20,7 +20,41 @@ int32_t scale_layout(int32_t kernel) {
 }
 
 bool kernel_ok(int32_t kernel) {
-  return kernel == MOE_GEMM_TOKEN_TILES || kernel == MOE_GEMM_WEIGHT_TILES;
+  return kernel == MOE_GEMM_TOKEN_TILES || kernel == MOE_GEMM_WEIGHT_TILES ||
+         kernel == MOE_GEMM_PAIR_TILES;
+}
+
+// The pair tiles cover 256 weight rows per tile: gate/up rows in steps of
+// 256 of I (stage 1), output features in steps of 256 of d (stage 2).
+bool pair_shape_ok(int32_t d, int32_t I) { return d % 256 == 0 && I % 256 == 0; }
+
+// Stage 1 / stage 2 of a family on the given device pointers.
+cudaError_t launch_w13(int32_t kernel, const uint8_t* xq, const uint8_t* xs, const int* counts,
+                       const int* offsets, int E, int d, int I, const uint8_t* w13,
+                       const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs, int64_t rows_capacity,
+                       int* status, cudaStream_t st) {
+  if (kernel == MOE_GEMM_WEIGHT_TILES)
+    return moe::launch_gemm_decode_w13_glu(xq, xs, counts, offsets, E, d, I, w13, w13_sf, hq, hs,
+                                           rows_capacity, status, st);
+  if (kernel == MOE_GEMM_PAIR_TILES)
+    return moe::launch_gemm_pair_w13_glu(xq, xs, counts, offsets, E, d, I, w13, w13_sf, hq, hs,
+                                         rows_capacity, status, st);
+  return moe::launch_gemm_w13_glu(xq, xs, counts, offsets, E, d, I, w13, w13_sf, hq, hs,
+                                  rows_capacity, status, st);
+}
+
+cudaError_t launch_w2(int32_t kernel, const uint8_t* hq, const uint8_t* hs, const int* counts,
+                      const int* offsets, int E, int I, int d, const uint8_t* w2,
+                      const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity, int* status,
+                      cudaStream_t st) {
+  if (kernel == MOE_GEMM_WEIGHT_TILES)
+    return moe::launch_gemm_decode_w2(hq, hs, counts, offsets, E, I, d, w2, w2_sf, yp,
+                                      rows_capacity, status, st);
+  if (kernel == MOE_GEMM_PAIR_TILES)
+    return moe::launch_gemm_pair_w2(hq, hs, counts, offsets, E, I, d, w2, w2_sf, yp,
+                                    rows_capacity, status, st);
+  return moe::launch_gemm_w2(hq, hs, counts, offsets, E, I, d, w2, w2_sf, yp, rows_capacity,
+                             status, st);
 }
 
 // The grouped-GEMM kernels moe_forward uses for MOE_GEMM_AUTO. Measured on
@@ -296,13 +330,10 @@ moe_status moe_grouped_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const 
   moe_status s = check_gemm_args(E, d, I, kernel, rows_capacity, xq, xs, counts, offsets, w13,
                                  w13_sf, hq, hs, true, ws, ws_bytes);
   if (s != MOE_OK) return s;
+  if (kernel == MOE_GEMM_PAIR_TILES && !pair_shape_ok(d, I)) return MOE_ERR_UNSUPPORTED;
   if (rows_capacity == 0) return MOE_OK;
-  if (kernel == MOE_GEMM_WEIGHT_TILES)
-    return from_cuda(moe::launch_gemm_decode_w13_glu(xq, xs, counts, offsets, E, d, I, w13,
-                                                     w13_sf, hq, hs, rows_capacity,
-                                                     static_cast<int*>(ws), stream));
-  return from_cuda(moe::launch_gemm_w13_glu(xq, xs, counts, offsets, E, d, I, w13, w13_sf, hq,
-                                            hs, rows_capacity, static_cast<int*>(ws), stream));
+  return from_cuda(launch_w13(kernel, xq, xs, counts, offsets, E, d, I, w13, w13_sf, hq, hs,
+                              rows_capacity, static_cast<int*>(ws), stream));
 }
 
 moe_status moe_grouped_gemm_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs,
@@ -331,12 +362,10 @@ moe_status moe_grouped_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int32
   moe_status s = check_gemm_args(E, I, d, kernel, rows_capacity, hq, hs, counts, offsets, w2,
                                  w2_sf, yp, nullptr, false, ws, ws_bytes);
   if (s != MOE_OK) return s;
+  if (kernel == MOE_GEMM_PAIR_TILES && !pair_shape_ok(d, I)) return MOE_ERR_UNSUPPORTED;
   if (rows_capacity == 0) return MOE_OK;
-  if (kernel == MOE_GEMM_WEIGHT_TILES)
-    return from_cuda(moe::launch_gemm_decode_w2(hq, hs, counts, offsets, E, I, d, w2, w2_sf, yp,
-                                                rows_capacity, static_cast<int*>(ws), stream));
-  return from_cuda(moe::launch_gemm_w2(hq, hs, counts, offsets, E, I, d, w2, w2_sf, yp,
-                                       rows_capacity, static_cast<int*>(ws), stream));
+  return from_cuda(launch_w2(kernel, hq, hs, counts, offsets, E, I, d, w2, w2_sf, yp,
+                             rows_capacity, static_cast<int*>(ws), stream));
 }
 
 moe_status moe_gemm_bf16(const uint16_t* a, const uint16_t* b, int64_t M, int32_t N, int32_t K,
@@ -445,6 +474,8 @@ moe_status forward_impl(bool a4w4, const moe_dims* dims, int32_t kernel, const u
   if (a4w4 && dims->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
   if (kernel == MOE_GEMM_AUTO) kernel = auto_kernel(dims->T, dims->E, dims->k);
   if (!kernel_ok(kernel)) return MOE_ERR_UNSUPPORTED;
+  if (kernel == MOE_GEMM_PAIR_TILES && !pair_shape_ok(dims->d, dims->I))
+    return MOE_ERR_UNSUPPORTED;
   const int32_t pad_m = group_pad(a4w4 ? int32_t(MOE_GEMM_TOKEN_TILES) : kernel);
   const moe_dims D = *dims;
   if (D.T == 0) return MOE_OK;
@@ -488,34 +519,20 @@ moe_status forward_impl(bool a4w4, const moe_dims* dims, int32_t kernel, const u
                                            W->w13_sf, hq, hs, scale_layout(kernel), L.rows_cap,
                                            status, stream)) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if (kernel == MOE_GEMM_WEIGHT_TILES)
-      e = moe::launch_gemm_decode_w2(hq, hs, counts, offsets, D.E, D.I, D.d, W->w2, W->w2_sf, yp,
-                                     L.rows_cap, status, stream);
-    else
-      e = moe::launch_gemm_w2(hq, hs, counts, offsets, D.E, D.I, D.d, W->w2, W->w2_sf, yp,
-                              L.rows_cap, status, stream);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if ((e = launch_w2(kernel, hq, hs, counts, offsets, D.E, D.I, D.d, W->w2, W->w2_sf, yp,
+                       L.rows_cap, status, stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
     return from_cuda(moe::launch_combine(yp, s2r, w, D.T, D.k, D.d, y, stream));
   }
   if ((e = moe::launch_quant_mxfp8(x, D.T, D.d, s2r, D.k, xq, xs, scale_layout(kernel),
                                    stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (kernel == MOE_GEMM_WEIGHT_TILES) {
-    if ((e = moe::launch_gemm_decode_w13_glu(xq, xs, counts, offsets, D.E, D.d, D.I, W->w13,
-                                             W->w13_sf, hq, hs, L.rows_cap, status, stream)) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-    if ((e = moe::launch_gemm_decode_w2(hq, hs, counts, offsets, D.E, D.I, D.d, W->w2, W->w2_sf,
-                                        yp, L.rows_cap, status, stream)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-  } else {
-    if ((e = moe::launch_gemm_w13_glu(xq, xs, counts, offsets, D.E, D.d, D.I, W->w13, W->w13_sf,
-                                      hq, hs, L.rows_cap, status, stream)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    if ((e = moe::launch_gemm_w2(hq, hs, counts, offsets, D.E, D.I, D.d, W->w2, W->w2_sf, yp,
-                                 L.rows_cap, status, stream)) != cudaSuccess)
-      return MOE_ERR_CUDA;
-  }
+  if ((e = launch_w13(kernel, xq, xs, counts, offsets, D.E, D.d, D.I, W->w13, W->w13_sf, hq, hs,
+                      L.rows_cap, status, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((e = launch_w2(kernel, hq, hs, counts, offsets, D.E, D.I, D.d, W->w2, W->w2_sf, yp,
+                     L.rows_cap, status, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return from_cuda(moe::launch_combine(yp, s2r, w, D.T, D.k, D.d, y, stream));
 }
 

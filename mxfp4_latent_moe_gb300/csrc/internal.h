@@ -80,6 +80,16 @@ cudaError_t launch_gemm_decode_w2(const uint8_t* hq, const uint8_t* hs, const in
                                   const int* offsets, int E, int I, int d, const uint8_t* w2,
                                   const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity,
                                   int* status, cudaStream_t st);
+// CTA-pair tiles (gemm_pair.cu): weights on M over two SMs, tokens on N;
+// groups of 128 rows, TILED activation scales; d % 256 == 0, I % 256 == 0.
+cudaError_t launch_gemm_pair_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,
+                                     const int* offsets, int E, int d, int I, const uint8_t* w13,
+                                     const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
+                                     int64_t rows_capacity, int* status, cudaStream_t st);
+cudaError_t launch_gemm_pair_w2(const uint8_t* hq, const uint8_t* hs, const int* counts,
+                                const int* offsets, int E, int I, int d, const uint8_t* w2,
+                                const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity,
+                                int* status, cudaStream_t st);
 // Dense BF16 GEMM C = A . B^T (gemm_bf16.cu); epilogues as moe_gemm_epilogue.
 enum GemmEpilogue : int { kEpiF32 = 0, kEpiBf16 = 1, kEpiSwiglu = 2 };
 int bf16_k_splits(int64_t M, int N, int K, int epilogue);

@@ -59,6 +59,25 @@ def test_forward_small_all_outputs(abi, orc, wl, kernel):
     gu.assert_layer_close(gu.bf16_to_f64(y), ref["y64"])
 
 
+@pytest.mark.parametrize("wl", [
+    synth.shape("pair_small", T=300, d=512, E=24, k=6, I=512),
+    synth.shape("pair_skewed", T=700, d=256, E=16, k=4, I=256, skew=True),
+    synth.shape("pair_one_expert", T=300, d=256, E=1, k=1, I=256),
+    synth.shape("pair_outliers", T=200, d=256, E=8, k=8, I=512, outlier_frac=0.05),
+])
+def test_forward_pair_tiles_small_all_outputs(abi, orc, wl):
+    """The CTA-pair family (weights on the M side of a 2-CTA MMA) on shapes
+    whose experts hold several 128- and 256-token chunks and a ragged last
+    chunk, every output element."""
+    L = synth.make_layer(wl, seed=0, device="cuda")
+    y, ids, w = _run_forward(abi, wl, L, abi.GEMM_PAIR_TILES)
+    H = _host_layer(L)
+    ref = orc.moe_forward(synth.bf16_bits(L["x"]), L["logits"].cpu().numpy(), wl.k, H["w13"],
+                          H["w13_s"], H["w2"], H["w2_s"], want_y64=True)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    gu.assert_layer_close(gu.bf16_to_f64(y), ref["y64"], wl.name)
+
+
 def test_forward_k0_gives_zeros_and_t0_is_a_noop(abi):
     wl = synth.shape("k0", T=16, d=128, E=4, k=0, I=128)
     L = synth.make_layer(wl, seed=0, device="cuda")
@@ -129,9 +148,13 @@ def _compared_tokens(wl, L):
 
 @pytest.mark.parametrize("name,kernel", [("decode_t64", 0), ("decode_t64", 1),
                                          ("decode_t512", 0), ("decode_t512", 1),
+                                         ("decode_t512", 3),
                                          ("prefill_skewed_t8192", 0), ("prefill_skewed_t8192", 2),
+                                         ("prefill_skewed_t8192", 1), ("prefill_skewed_t8192", 3),
                                          ("prefill_outlier_t32768", 0),
-                                         ("prefill_outlier_t32768", 2)])
+                                         ("prefill_outlier_t32768", 2),
+                                         ("prefill_outlier_t32768", 1),
+                                         ("prefill_outlier_t32768", 3)])
 def test_forward_full_size_workloads(abi, orc, name, kernel):
     """The benchmark's configuration (kernel family 0 = moe_default_kernel:
     weight tiles at decode, token tiles at prefill), and each workload through

@@ -1,10 +1,12 @@
 """GPU parity of the two grouped GEMMs (tcgen05 block-scaled MMA) against the
 oracle's per-expert stage functions, on ragged expert groups: empty groups,
 groups of 1, 15..17, 127..129 and several hundred rows, K not a multiple of the
-pipeline depth, and more tiles than SMs. Both kernel families: token tiles
-(tokens on the MMA's M side, groups padded to 128, TILED activation scales)
-and weight tiles (weights on the M side, tokens as N = 32 per tile, groups
-padded to 32, GROUP32 activation scales)."""
+pipeline depth, and more tiles than SMs. All three kernel families: token
+tiles (tokens on the MMA's M side, groups padded to 128, TILED activation
+scales), weight tiles (weights on the M side, tokens as N = 32 per tile,
+groups padded to 32, GROUP32 activation scales) and pair tiles (weights on the
+M side of a 2-CTA MMA, tokens as N in chunks of 128 / 256 with a ragged last
+chunk, groups padded to 128, TILED scales; d and I multiples of 256)."""
 import numpy as np
 import pytest
 import torch
@@ -20,8 +22,12 @@ def abi():
     return gu.cuda_lib()
 
 
+def _layout(kernel):
+    return 1 if kernel == 2 else 0       # GROUP32 for weight tiles, else TILED
+
+
 def _groups(sizes, kernel):
-    pad = 128 if kernel == 1 else 32
+    pad = 32 if kernel == 2 else 128
     offsets = [0]
     for c in sizes:
         offsets.append(offsets[-1] + (c + pad - 1) // pad * pad)
@@ -31,11 +37,11 @@ def _groups(sizes, kernel):
 
 
 def _act_scales(canon, K, kernel):
-    return gu.tile(canon, K) if kernel == 1 else gu.tile_g32(canon, K)
+    return gu.tile_g32(canon, K) if kernel == 2 else gu.tile(canon, K)
 
 
 def _act_untile(buf, rows, K, kernel):
-    return gu.untile(buf, rows, K) if kernel == 1 else gu.untile_g32(buf, rows, K)
+    return gu.untile_g32(buf, rows, K) if kernel == 2 else gu.untile(buf, rows, K)
 
 
 def _dev(a):
@@ -75,13 +81,21 @@ CASES = [
     ([0, 1, 15, 16, 17, 127, 128, 129, 300], 256, 256),
     ([3, 0, 250, 130, 33, 64, 96, 65], 384, 384),
     (list(np.random.default_rng(0).integers(0, 300, 40)), 256, 512),
+    # several token chunks per expert for the pair tiles (128 / 256 wide)
+    ([0, 255, 256, 257, 1, 600, 383, 384, 31], 512, 512),
 ]
 
 
+def _supported(kernel, d, I):
+    if kernel == 3 and (d % 256 or I % 256):
+        pytest.skip("pair tiles need d and I multiples of 256")
+
+
 @pytest.mark.parametrize("out_off", [0, 16])   # bytes: 32-byte-aligned output, or 16 only
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 @pytest.mark.parametrize("sizes,d,I", CASES)
 def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel, out_off):
+    _supported(kernel, d, I)
     counts, offsets, rows, rc = _groups(sizes, kernel)
     E = len(sizes)
     W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=1)
@@ -89,7 +103,7 @@ def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel, out_off):
     xs = synth.random_scale_codes((rc, d // 32), lo=118, hi=130, seed=3).numpy()
     hq = torch.full((rc * I + out_off,), 0x5A, dtype=torch.uint8, device="cuda")[out_off:]
     hq = hq.view(rc, I)
-    hs = torch.full((abi.moe_activation_scale_bytes(rc, I, kernel - 1),), 0x5A,
+    hs = torch.full((abi.moe_activation_scale_bytes(rc, I, _layout(kernel)),), 0x5A,
                     dtype=torch.uint8, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     abi.moe_grouped_gemm_w13_glu(_dev(xq), _dev(_act_scales(xs, d, kernel)), _dev(counts),
@@ -111,9 +125,10 @@ def test_w13_glu_matches_oracle_stage1(abi, orc, sizes, d, I, kernel, out_off):
 
 
 @pytest.mark.parametrize("out_off", [0, 16])   # bytes: 32-byte-aligned output, or 16 only
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 @pytest.mark.parametrize("sizes,d,I", CASES)
 def test_w2_matches_oracle_stage2(abi, orc, sizes, d, I, kernel, out_off):
+    _supported(kernel, d, I)
     counts, offsets, rows, rc = _groups(sizes, kernel)
     E = len(sizes)
     W = synth.make_weights(synth.shape("g", T=1, d=d, E=E, k=1, I=I), seed=4)
@@ -154,9 +169,23 @@ def test_gemm_refuses_bad_groups(abi):
            (np.array([130, 0], np.int32), np.array([0, 128, 256], np.int32)),   # count > group
            (np.array([1, 1], np.int32), np.array([0, 128, 384], np.int32))]     # past the capacity
     for counts, offsets in bad:
-        for kernel in (1, 2):
+        for kernel in (1, 2, 3):
             ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
             abi.moe_grouped_gemm_w13_glu(xq, xs, _dev(counts), _dev(offsets), 2, d, I, kernel,
                                          w13_boxed, w13_sf, hq, hs, rc, ws)
             assert abi.moe_check_device_status(ws) == 6       # MOE_ERR_DEVICE_BAD_INPUT
     assert bool((hq == 0x5A).all())                           # nothing written
+
+
+def test_pair_tiles_refuse_widths_not_multiples_of_256(abi):
+    d, I, E, rc = 384, 256, 2, 256
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    z = lambda n: torch.zeros(n, dtype=torch.uint8, device="cuda")
+    counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    with pytest.raises(abi.MoeError) as err:
+        abi.moe_grouped_gemm_w13_glu(z(rc * d), z(abi.moe_tiled_scale_bytes(rc, d)), counts,
+                                     offsets, E, d, I, 3, z(E * 2 * I * d // 2),
+                                     z(abi.moe_tiled_scale_bytes(E * 2 * I, d)), z(rc * I),
+                                     z(abi.moe_tiled_scale_bytes(rc, I)), rc, ws)
+    assert err.value.code == abi.UNSUPPORTED
