@@ -603,6 +603,34 @@ def measure_layer(args, wl, dev, sampler, a4w4=False):
     if abi.moe_check_device_status(gws) != abi.OK or abi.moe_check_device_status(pws) != abi.OK:
         raise RuntimeError("device status error in the kernel breakdown (%s)" % wl.name)
 
+    # ---- the step as one CUDA graph, replayed back to back (device-resident):
+    # graph time minus the two GEMMs' event times bounds what folding the
+    # other kernels into the GEMMs (a single-launch layer) could save
+    graph, _, _ = layer.capture(x, logits, ws=ws, y=y, a4w4=a4w4)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if flush is None:
+        g0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = g0.elapsed_time(g1) / args.steps
+    else:
+        gev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            gev[2 * i].record(stream)
+            graph.replay()
+            gev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        graph_ms = sum(gev[2 * i].elapsed_time(gev[2 * i + 1]) for i in range(args.steps)) / args.steps
+    del graph
+    if abi.moe_check_device_status(ws) != abi.OK:
+        raise RuntimeError("device status error in the graph replays (%s)" % wl.name)
+
     peaks, peak_src = load_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -662,6 +690,10 @@ def measure_layer(args, wl, dev, sampler, a4w4=False):
                                   "stage-1 peak + 2TkdI FLOP / (bf16_tflops x 2))"},
         "roofline": roof,
         "kernels_ms": kms,
+        "graph_ms_per_step": graph_ms,
+        "outside_gemms_ms": graph_ms - kms["gemm_w13_glu"] - kms["gemm_w2"],
+        "outside_gemms_how": "step replayed as one CUDA graph minus the two GEMMs' mean event "
+                             "times: the most a single-launch layer could save",
         "gpu_launches": launches_per_step * args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1),
         "l2": l2_note,
@@ -844,6 +876,8 @@ def main():
         "layer_roofline": head["layer_roofline"],
         "roofline": head["roofline"],
         "kernels_ms": head["kernels_ms"],
+        "graph_ms_per_step": head["graph_ms_per_step"],
+        "outside_gemms_ms": head["outside_gemms_ms"],
         "gpu_launches": head["gpu_launches"],
         "e2e": e2e["e2e"],
         "e2e_serial": e2e["e2e_serial"],
