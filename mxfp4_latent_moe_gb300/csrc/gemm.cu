@@ -112,15 +112,6 @@ __device__ __forceinline__ void st_global_32B(void* dst, uint32_t a0, uint32_t a
 }
 
 // ---- 2-CTA clusters: the A tile multicast to both CTAs of a pair ----------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-                   "memory");
-}
 // TMA load delivered to the same shared-memory offset (and mbarrier) in every
 // CTA of `mask`.
 __device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar,
@@ -694,6 +685,23 @@ bool encode_boxed_weights_packed(CUtensorMap* map, const void* base, int64_t row
   const CUresult r =
       fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// A TILED scale array of `bytes` bytes as a 2-D map of 128-byte rows, boxes
+// of 4 rows (one 512-byte atom), no swizzle. Rows past the array are zero
+// filled, so an atom of a tile row past the groups reads as zeros.
+bool encode_scale_atoms(CUtensorMap* map, const void* base, int64_t bytes) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn || bytes <= 0 || bytes % 512 != 0) return false;
+  const cuuint64_t dims[2] = {128u, cuuint64_t(bytes / 128)};
+  const cuuint64_t strides[1] = {128u};
+  const cuuint32_t box[2] = {128u, 4u};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

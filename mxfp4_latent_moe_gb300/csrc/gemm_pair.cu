@@ -120,111 +120,6 @@ struct PairParams {
   int* status;
 };
 
-// ---- 2-CTA (cta_group::2) forms ------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-          "memory");
-}
-// Address of the same shared-memory variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-// 2-D TMA load into this CTA's shared memory whose bytes complete on the
-// mbarrier at cluster address `bar` (this CTA's or its pair partner's).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
-                                                 uint32_t bar, int32_t x, int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-// Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-// try_wait with acquire at cluster scope (the phase may complete by arrivals
-// from the other CTA of the pair).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0u;
-}
-__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t* bar, uint32_t parity,
-                                                       volatile int* abort) {
-  bool ok = mbar_try_wait_cluster(bar, parity);
-  if (!ok) {
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-      if (mbar_try_wait_cluster(bar, parity)) {
-        ok = true;
-        break;
-      }
-      if ((i & 31u) == 0u) {
-        if (abort && *abort) break;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-      }
-    }
-  }
-  return __all_sync(0xffffffffu, ok);
-}
-__device__ __forceinline__ void tmem_alloc2(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish2() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-// Copies a 32-row x 16-byte scale block of each CTA's shared memory into its
-// own tensor memory at columns [taddr, taddr+4).
-__device__ __forceinline__ void tc_cp2(uint32_t taddr, uint64_t src_desc) {
-  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc)
-               : "memory");
-}
-// D (both CTAs' tensor memory) (+)= A (128 rows in each CTA) x B (N/2 rows in
-// each CTA)^T with per-32 E8M0 scales.
-__device__ __forceinline__ void tc_mma_mx2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
-      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-      : "memory");
-}
-// Arrives once on the mbarrier at the same offset in every CTA of `mask` when
-// all tcgen05 operations the thread issued before it have completed.
-__device__ __forceinline__ void tc_commit2_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
 // Unit -> (expert, weight tile, first token row, tokens). An expert has
 // ceil(counts[e]/NTOK) token chunks; the chunk index runs fastest.
 template <int NTOK>
@@ -560,22 +455,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after();
   if (warp == 1) tmem_dealloc2(tmem_base, kTmemCols);
-}
-
-// A TILED scale array of `bytes` bytes as a 2-D map of 128-byte rows, boxes
-// of 4 rows (one 512-byte atom), no swizzle.
-bool encode_scale_atoms(CUtensorMap* map, const void* base, int64_t bytes) {
-  EncodeTiledFn fn = encode_tiled_fn();
-  if (!fn || bytes <= 0 || bytes % 512 != 0) return false;
-  const cuuint64_t dims[2] = {128u, cuuint64_t(bytes / 128)};
-  const cuuint64_t strides[1] = {128u};
-  const cuuint32_t box[2] = {128u, 4u};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r =
-      fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
 }
 
 template <int MODE>

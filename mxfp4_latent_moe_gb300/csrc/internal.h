@@ -69,6 +69,8 @@ EncodeTiledFn encode_tiled_fn();   // cuTensorMapEncodeTiled through the runtime
 bool encode_operand(CUtensorMap* map, const void* base, bool e2m1, int K, int64_t rows,
                     int box_rows);
 bool encode_boxed_weights(CUtensorMap* map, const void* base, int64_t rows, int K);
+// A TILED scale array as rows of 128 bytes, boxes of one 512-byte atom.
+bool encode_scale_atoms(CUtensorMap* map, const void* base, int64_t bytes);
 int sm_count();
 
 cudaError_t launch_gemm_decode_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,
