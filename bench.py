@@ -633,12 +633,24 @@ def measure_layer(args, wl, dev, sampler, a4w4=False):
 
     peaks, peak_src = load_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    bf16_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     bf16_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    tensor_peak = bf16_peak * FP8_OVER_BF16
-    w13_peak = bf16_peak * (FP4_OVER_BF16 if a4w4 else FP8_OVER_BF16)
+    # The tensor peak of the regime the timed region ran in: the sustained
+    # (power-capped) bf16 figure when the GPU reported sw_power_cap during the
+    # timed steps, the burst figure otherwise. Both fractions are reported.
+    clocks = sampler.summary(t_wall0, t_wall1)
+    capped = "sw_power_cap" in clocks.get("reasons", [])
+    bf16_peak = bf16_sus if capped else bf16_burst
+    regime = "sustained (sw_power_cap during the timed steps)" if capped else "burst"
+    w13_ratio = FP4_OVER_BF16 if a4w4 else FP8_OVER_BF16
+
+    def math_time(bf16):
+        return (4.0 * T * k * d * I / (bf16 * w13_ratio * 1e12) +
+                2.0 * T * k * d * I / (bf16 * FP8_OVER_BF16 * 1e12))
+
+    w13_peak = bf16_peak * w13_ratio
     t_mem = U * expert_bytes / (hbm_peak * 1e9)
-    t_math = 4.0 * T * k * d * I / (w13_peak * 1e12) + 2.0 * T * k * d * I / (tensor_peak * 1e12)
+    t_math = math_time(bf16_peak)
     bound = "hbm" if t_mem >= t_math else "tensor"
     ms_per_step = total_ms / args.steps
     layer_frac = max(t_mem, t_math) / (ms_per_step / 1e3)
@@ -662,14 +674,15 @@ def measure_layer(args, wl, dev, sampler, a4w4=False):
         roof = {"kernel": dom, "bound": "tensor", "achieved": dom_flops / dom_s / 1e12,
                 "peak": w13_peak, "unit": "TFLOP/s",
                 "frac": dom_flops / dom_s / 1e12 / w13_peak,
+                "frac_of_burst": dom_flops / dom_s / 1e12 / (bf16_burst * ratio),
                 "frac_of_sustained": dom_flops / dom_s / 1e12 / (bf16_sus * ratio),
                 "traffic": profiled_traffic(dom, wl.name, family) if not a4w4 else None,
                 "algorithmic_flops": dom_flops,
                 "algorithmic_flops_how": "4*T*k*d*I (gate and up products of the routed rows; "
                                          "padding rows not credited)",
                 "mean_ms": kms[dom],
-                "peak_source": peak_src + " bf16_tflops (burst) x %.1f (nominal %s / bf16 dense "
-                               "ratio)" % (ratio, what)}
+                "peak_source": "%s bf16 %s x %.1f (nominal %s / bf16 dense ratio)"
+                               % (peak_src, regime, ratio, what)}
         if a4w4:
             mma_peak = bf16_peak * FP4_MMA_OVER_BF16
             roof["frac_of_measured_mma_rate"] = dom_flops / dom_s / 1e12 / mma_peak
@@ -681,13 +694,16 @@ def measure_layer(args, wl, dev, sampler, a4w4=False):
         "gemm_kernel": family, "touched_experts": U, "padded_rows": padded_rows,
         "layer_roofline": {"bound": bound, "time_ms": 1e3 * max(t_mem, t_math),
                            "frac": layer_frac,
-                           "frac_of_sustained": (max(t_mem, t_math) if bound == "hbm" else
-                                                 t_math * bf16_peak / bf16_sus)
+                           "frac_of_burst": max(t_mem, math_time(bf16_burst))
                            / (ms_per_step / 1e3),
+                           "frac_of_sustained": max(t_mem, math_time(bf16_sus))
+                           / (ms_per_step / 1e3),
+                           "tensor_peak_regime": regime,
                            "tflops": flops / (ms_per_step / 1e3) / 1e12,
                            "weight_gbs": U * expert_bytes / (ms_per_step / 1e3) / 1e9,
                            "how": "max(touched experts x 17,547,264 B / hbm_gbs, 4TkdI FLOP / "
-                                  "stage-1 peak + 2TkdI FLOP / (bf16_tflops x 2))"},
+                                  "stage-1 peak + 2TkdI FLOP / (bf16 peak x 2)), bf16 peak of "
+                                  "the regime"},
         "roofline": roof,
         "kernels_ms": kms,
         "graph_ms_per_step": graph_ms,
@@ -695,7 +711,7 @@ def measure_layer(args, wl, dev, sampler, a4w4=False):
         "outside_gemms_how": "step replayed as one CUDA graph minus the two GEMMs' mean event "
                              "times: the most a single-launch layer could save",
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": sampler.summary(t_wall0, t_wall1),
+        "clocks": clocks,
         "l2": l2_note,
     }
     state = dict(L=L, layer=layer, ws=ws, y=y, flush=flush, stream=stream)

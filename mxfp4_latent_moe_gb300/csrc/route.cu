@@ -8,11 +8,20 @@
 // Each lane holds the logits of experts lane, lane+32, ... (up to 32 per lane
 // for E <= 1024) as 64-bit keys that order like (value desc, id asc): the
 // high word maps the float monotonically onto unsigned integers (-0 joins +0),
-// the low word is ~id. A lane keeps its two best untaken keys (branch-free
-// max/min updates); each of the k rounds takes the warp's best head with two
-// warp reductions (max of the high words, then max of the low words among the
-// lanes that hold it), and the owning lane pops it. Reads are coalesced: a
+// the low word is ~id, so all keys of a token differ. Reads are coalesced: a
 // token's row is read once.
+//
+// Fast path: t0 = the k-th largest of the 32 lane maxima. At least k keys are
+// >= t0 (the k lanes whose maximum is), so every one of the token's k largest
+// keys is >= t0; when at most 32 keys are, they are gathered one per lane and
+// sorted across the warp (bitonic network, 15 exchange steps), and lanes
+// 0..k-1 hold the picks in order. For N(0,1) logits at E = 896, k = 16 about
+// 22 keys pass on average and more than 32 for about 0.1% of tokens.
+// Otherwise (the general path): a lane keeps its two best untaken keys
+// (branch-free max/min updates); each of the k rounds takes the warp's best
+// head with two warp reductions (max of the high words, then max of the low
+// words among the lanes that hold it), and the owning lane pops it. Both paths
+// give the same, exact result.
 #include "internal.h"
 
 namespace moe {
@@ -50,10 +59,25 @@ __device__ __forceinline__ void lane_top2(const uint64_t (&key)[NPL], uint64_t l
   }
 }
 
+// Descending sort of one key per lane across the warp (lane 0 the largest).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  }
+  return v;
+}
+
 template <int NPL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                       int* __restrict__ ids, float* __restrict__ w) {
+  __shared__ uint64_t cand[kWarpsPerBlock * 32];   // fast-path candidates, 32 per warp
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -65,25 +89,52 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int e = lane + 32 * i;
     key[i] = e < E ? route_key(__ldg(row + e), e) : 0;
   }
-  // A lane gives up its keys in descending order, so once its two are taken
-  // it rescans for the best two below the last one it gave up.
-  uint64_t a, b;
-  lane_top2<NPL>(key, ~uint64_t(0), a, b);
   uint32_t my_hi = 0, my_lo = 0;
-  for (int j = 0; j < k; ++j) {
-    const uint32_t hi = uint32_t(a >> 32), lo = uint32_t(a);
-    const uint32_t m_hi = __reduce_max_sync(0xffffffffu, hi);
-    const uint32_t m_lo = __reduce_max_sync(0xffffffffu, hi == m_hi ? lo : 0u);
-    const int id = int(0xFFFFFFFFu - m_lo);
-    if ((id & 31) == lane) {   // this lane's head won: pop it
-      const uint64_t taken = a;
-      a = b;
-      b = 0;
-      if (a == 0) lane_top2<NPL>(key, taken, a, b);
-    }
-    if (lane == j) {
-      my_hi = m_hi;
-      my_lo = m_lo;
+  // fast path: the keys >= t0, one per lane, sorted across the warp
+  uint64_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) mx = key[i] > mx ? key[i] : mx;
+  const uint64_t t0 = __shfl_sync(0xffffffffu, warp_sort_desc(mx, lane), k - 1);
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) cnt += key[i] >= t0 ? 1 : 0;
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += n;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (total <= 32) {   // warp-uniform
+    uint64_t* slots = cand + (threadIdx.x >> 5) * 32;
+    int pos = incl - cnt;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (key[i] >= t0) slots[pos++] = key[i];
+    __syncwarp();
+    const uint64_t c = warp_sort_desc(lane < total ? slots[lane] : 0, lane);
+    my_hi = uint32_t(c >> 32);
+    my_lo = uint32_t(c);
+  } else {
+    // A lane gives up its keys in descending order, so once its two are
+    // taken it rescans for the best two below the last one it gave up.
+    uint64_t a, b;
+    lane_top2<NPL>(key, ~uint64_t(0), a, b);
+    for (int j = 0; j < k; ++j) {
+      const uint32_t hi = uint32_t(a >> 32), lo = uint32_t(a);
+      const uint32_t m_hi = __reduce_max_sync(0xffffffffu, hi);
+      const uint32_t m_lo = __reduce_max_sync(0xffffffffu, hi == m_hi ? lo : 0u);
+      const int id = int(0xFFFFFFFFu - m_lo);
+      if ((id & 31) == lane) {   // this lane's head won: pop it
+        const uint64_t taken = a;
+        a = b;
+        b = 0;
+        if (a == 0) lane_top2<NPL>(key, taken, a, b);
+      }
+      if (lane == j) {
+        my_hi = m_hi;
+        my_lo = m_lo;
+      }
     }
   }
   // sigmoid of the selected logits, renormalised over the k of them
