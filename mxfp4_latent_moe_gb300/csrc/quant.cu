@@ -8,11 +8,13 @@
 // clamp(floor(log2(amax)) - 8 + 127, 0, 254), and the elements are the E4M3
 // round-to-nearest-even of v * 2^(127 - code), saturated to +-448.
 //
-// Layout of the work: each thread owns 8 consecutive bf16 of one token (one
-// 16-byte load); 4 lanes share a 32-block (amax by two xor-shuffles) and 16
-// lanes a 128-input group whose four scale codes go out as one 32-bit word of
-// the TILED scale layout. The token is read once and written to each of its k
-// grouped rows (8-byte stores, 256 contiguous bytes per warp and row).
+// Layout of the work: each thread owns VEC consecutive bf16 of one token
+// (VEC/8 16-byte loads; VEC = 8 for small batches, 16 for large ones); the
+// 32/VEC lanes of a 32-block take its amax by xor-shuffles and the 128/VEC
+// lanes of a 128-input group send its four scale codes out as one 32-bit word
+// of the scale layout. The token is read once and written to each of its k
+// grouped rows (VEC codes per thread and row, 32 * VEC contiguous codes per
+// warp and row).
 #include "internal.h"
 
 namespace moe {
@@ -36,7 +38,7 @@ __device__ __forceinline__ void load_rows(const int* __restrict__ slot_to_row, i
     rows[q] = j0 + q >= nrows ? 0 : slot_to_row ? __ldg(slot_to_row + t * k + j0 + q) : int(t);
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float* f) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -45,95 +47,62 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& q, float (&f)[8]) {
   }
 }
 
-template <int LAYOUT, int kRowBatch>
+// MXFP8 (FP4 false: E4M3 elements, shared exponent floor(log2(amax)) - 8,
+// codes [rows][d]) or MXFP4 (FP4 true, the A4W4 stage-1 activations: E2M1
+// elements, shared exponent floor(log2(amax)) - 2, codes packed [rows][d/2]
+// with the even element in the low nibble of each byte).
+template <bool FP4, int LAYOUT, int kRowBatch, int VEC>
 __global__ void __launch_bounds__(kQuantThreads)
-    quant_mxfp8_kernel(const uint4* __restrict__ x, int d, const int* __restrict__ slot_to_row,
-                       int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                       int64_t total_vec) {
+    quant_mx_kernel(const uint4* __restrict__ x, int d, const int* __restrict__ slot_to_row,
+                    int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                    int64_t total_vec) {
+  static_assert(VEC == 8 || VEC == 16, "a thread owns 8 or 16 inputs");
+  constexpr int kLoads = VEC / 8;
+  constexpr int kBlockLanes = 32 / VEC;             // lanes of a 32-block
+  constexpr int kGroupLanes = 128 / VEC;            // lanes of a 128-input group
+  constexpr int kWords = FP4 ? VEC / 8 : VEC / 4;   // 32-bit code words per thread
   pdl_trigger();
   pdl_wait();
   const int64_t g = int64_t(blockIdx.x) * kQuantThreads + threadIdx.x;
   const int lane = threadIdx.x & 31;
   const bool valid = g < total_vec;
-  const int vpr = d >> 3;  // 8-element vectors per row
-  uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-  if (valid) raw = __ldg(x + g);
-  float f[8];
-  bf16x8_to_f32(raw, f);
-  float amax = 0.0f;
+  const int vpr = d / VEC;   // threads per token
+  float f[VEC];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  const int code = mx_scale_code(amax);
-  const float m = mx_scale_mult(code);
-  uint2 packed;
-  packed.x = e4m3x4(f[0], f[1], f[2], f[3], m);
-  packed.y = e4m3x4(f[4], f[5], f[6], f[7], m);
-  const int base = lane & ~15;
-  const uint32_t s0 = __shfl_sync(0xffffffffu, code, base);
-  const uint32_t s1 = __shfl_sync(0xffffffffu, code, base + 4);
-  const uint32_t s2 = __shfl_sync(0xffffffffu, code, base + 8);
-  const uint32_t s3 = __shfl_sync(0xffffffffu, code, base + 12);
-  if (!valid) return;
-  const uint32_t sword = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
-  const int64_t t = g / vpr;
-  const int v = int(g - t * vpr);
-  const int nrows = slot_to_row ? k : 1;
-  for (int j0 = 0; j0 < nrows; j0 += kRowBatch) {
-    int rows[kRowBatch];
-    load_rows<kRowBatch>(slot_to_row, t, k, nrows, j0, rows);
-#pragma unroll
-    for (int q = 0; q < kRowBatch; ++q) {
-      if (j0 + q >= nrows) break;
-      const int64_t row = rows[q];
-      *reinterpret_cast<uint2*>(codes + row * d + int64_t(v) * 8) = packed;
-      if ((lane & 15) == 0) {
-        const int64_t off = LAYOUT == kScalesGroup32 ? group32_sf_offset(row, int64_t(v >> 2), d)
-                                                     : tiled_sf_offset(row, int64_t(v >> 2), d);
-        *reinterpret_cast<uint32_t*>(scales + off) = sword;
-      }
-    }
+  for (int l = 0; l < kLoads; ++l) {
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (valid) raw = __ldg(x + g * kLoads + l);
+    bf16x8_to_f32(raw, f + 8 * l);
   }
-}
-
-// MXFP4 (the A4W4 stage-1 activations): the same work layout with E2M1
-// elements and shared exponent floor(log2(amax)) - 2; a thread's 8 codes are
-// one 32-bit word of the packed [rows][d/2] output (even element in the low
-// nibble of each byte).
-template <int LAYOUT, int kRowBatch>
-__global__ void __launch_bounds__(kQuantThreads)
-    quant_mxfp4_kernel(const uint4* __restrict__ x, int d, const int* __restrict__ slot_to_row,
-                       int k, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                       int64_t total_vec) {
-  pdl_trigger();
-  pdl_wait();
-  const int64_t g = int64_t(blockIdx.x) * kQuantThreads + threadIdx.x;
-  const int lane = threadIdx.x & 31;
-  const bool valid = g < total_vec;
-  const int vpr = d >> 3;
-  uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-  if (valid) raw = __ldg(x + g);
-  float f[8];
-  bf16x8_to_f32(raw, f);
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  const int code = mx_scale_code<2>(amax);
+  for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+  for (int s = 1; s < kBlockLanes; s <<= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, s));
+  const int code = FP4 ? mx_scale_code<2>(amax) : mx_scale_code(amax);
   const float m = mx_scale_mult(code);
-  const uint32_t packed = e2m1x2(f[0] * m, f[1] * m) | (e2m1x2(f[2] * m, f[3] * m) << 8) |
-                          (e2m1x2(f[4] * m, f[5] * m) << 16) | (e2m1x2(f[6] * m, f[7] * m) << 24);
-  const int base = lane & ~15;
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < kWords; ++i) {
+    if (FP4)
+      w[i] = e2m1x2(f[8 * i] * m, f[8 * i + 1] * m) | (e2m1x2(f[8 * i + 2] * m, f[8 * i + 3] * m) << 8) |
+             (e2m1x2(f[8 * i + 4] * m, f[8 * i + 5] * m) << 16) |
+             (e2m1x2(f[8 * i + 6] * m, f[8 * i + 7] * m) << 24);
+    else
+      w[i] = e4m3x4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3], m);
+  }
+  const int base = lane & ~(kGroupLanes - 1);
   const uint32_t s0 = __shfl_sync(0xffffffffu, code, base);
-  const uint32_t s1 = __shfl_sync(0xffffffffu, code, base + 4);
-  const uint32_t s2 = __shfl_sync(0xffffffffu, code, base + 8);
-  const uint32_t s3 = __shfl_sync(0xffffffffu, code, base + 12);
+  const uint32_t s1 = __shfl_sync(0xffffffffu, code, base + kBlockLanes);
+  const uint32_t s2 = __shfl_sync(0xffffffffu, code, base + 2 * kBlockLanes);
+  const uint32_t s3 = __shfl_sync(0xffffffffu, code, base + 3 * kBlockLanes);
   if (!valid) return;
   const uint32_t sword = s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
   const int64_t t = g / vpr;
   const int v = int(g - t * vpr);
+  const int64_t row_bytes = FP4 ? d >> 1 : d;
+  const int64_t blk = int64_t(v) * VEC / 32;   // first 32-block of the thread
   const int nrows = slot_to_row ? k : 1;
   for (int j0 = 0; j0 < nrows; j0 += kRowBatch) {
     int rows[kRowBatch];
@@ -142,10 +111,16 @@ __global__ void __launch_bounds__(kQuantThreads)
     for (int q = 0; q < kRowBatch; ++q) {
       if (j0 + q >= nrows) break;
       const int64_t row = rows[q];
-      *reinterpret_cast<uint32_t*>(codes + row * (d >> 1) + int64_t(v) * 4) = packed;
-      if ((lane & 15) == 0) {
-        const int64_t off = LAYOUT == kScalesGroup32 ? group32_sf_offset(row, int64_t(v >> 2), d)
-                                                     : tiled_sf_offset(row, int64_t(v >> 2), d);
+      uint8_t* dst = codes + row * row_bytes + int64_t(v) * (4 * kWords);
+      if (kWords == 4)
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      else if (kWords == 2)
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+      else
+        *reinterpret_cast<uint32_t*>(dst) = w[0];
+      if ((lane & (kGroupLanes - 1)) == 0) {
+        const int64_t off = LAYOUT == kScalesGroup32 ? group32_sf_offset(row, blk, d)
+                                                     : tiled_sf_offset(row, blk, d);
         *reinterpret_cast<uint32_t*>(scales + off) = sword;
       }
     }
@@ -188,36 +163,33 @@ __global__ void prepack_weights_kernel(const uint4* __restrict__ src, int K,
 
 namespace {
 
-template <int LAYOUT, int B>
-cudaError_t launch_quant_kernel(bool fp4, dim3 grid, cudaStream_t st, const uint4* x, int d,
-                                const int* slot_to_row, int k, uint8_t* codes, uint8_t* scales,
-                                int64_t total) {
-  const bool pdl = B == 16;   // decode-sized
-  if (fp4)
-    return launch_ex(pdl, quant_mxfp4_kernel<LAYOUT, B>, grid, dim3(kQuantThreads), 0, st, 1, x,
-                     d, slot_to_row, k, codes, scales, total);
-  return launch_ex(pdl, quant_mxfp8_kernel<LAYOUT, B>, grid, dim3(kQuantThreads), 0, st, 1, x, d,
-                   slot_to_row, k, codes, scales, total);
+template <bool FP4, int LAYOUT>
+cudaError_t launch_quant_layout(const uint16_t* x, int64_t T, int d, const int* slot_to_row, int k,
+                                uint8_t* codes, uint8_t* scales, cudaStream_t st) {
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  const int64_t total8 = T * (d / 8);
+  const dim3 grid8(static_cast<unsigned>((total8 + kQuantThreads - 1) / kQuantThreads));
+  if (total8 <= kSmallBatchThreads)   // decode-sized: PDL, 16 rows looked up at once
+    return launch_ex(true, quant_mx_kernel<FP4, LAYOUT, 16, 8>, grid8, dim3(kQuantThreads), 0, st,
+                     1, xv, d, slot_to_row, k, codes, scales, total8);
+  // 16 inputs a thread: 16-byte MXFP8 code stores want a 16-byte aligned output
+  if (!FP4 && reinterpret_cast<uintptr_t>(codes) % 16 != 0)
+    return launch_ex(false, quant_mx_kernel<FP4, LAYOUT, kLargeBatch, 8>, grid8,
+                     dim3(kQuantThreads), 0, st, 1, xv, d, slot_to_row, k, codes, scales, total8);
+  const int64_t total = T * (d / 16);
+  const dim3 grid(static_cast<unsigned>((total + kQuantThreads - 1) / kQuantThreads));
+  return launch_ex(false, quant_mx_kernel<FP4, LAYOUT, kLargeBatch, 16>, grid,
+                   dim3(kQuantThreads), 0, st, 1, xv, d, slot_to_row, k, codes, scales, total);
 }
 
 cudaError_t launch_quant(bool fp4, const uint16_t* x, int T, int d, const int* slot_to_row, int k,
                          uint8_t* codes, uint8_t* scales, int layout, cudaStream_t st) {
-  const int64_t total = int64_t(T) * (d / 8);
-  if (total == 0 || (slot_to_row && k == 0)) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>((total + kQuantThreads - 1) / kQuantThreads));
-  const uint4* xv = reinterpret_cast<const uint4*>(x);
-  const bool small = total <= kSmallBatchThreads;
+  if (int64_t(T) * d == 0 || (slot_to_row && k == 0)) return cudaSuccess;
   if (layout == kScalesGroup32)
-    return small ? launch_quant_kernel<kScalesGroup32, 16>(fp4, grid, st, xv, d, slot_to_row, k,
-                                                           codes, scales, total)
-                 : launch_quant_kernel<kScalesGroup32, kLargeBatch>(fp4, grid, st, xv, d,
-                                                                    slot_to_row, k, codes,
-                                                                    scales, total);
-  return small ? launch_quant_kernel<kScalesTiled128, 16>(fp4, grid, st, xv, d, slot_to_row, k,
-                                                          codes, scales, total)
-               : launch_quant_kernel<kScalesTiled128, kLargeBatch>(fp4, grid, st, xv, d,
-                                                                   slot_to_row, k, codes, scales,
-                                                                   total);
+    return fp4 ? launch_quant_layout<true, kScalesGroup32>(x, T, d, slot_to_row, k, codes, scales, st)
+               : launch_quant_layout<false, kScalesGroup32>(x, T, d, slot_to_row, k, codes, scales, st);
+  return fp4 ? launch_quant_layout<true, kScalesTiled128>(x, T, d, slot_to_row, k, codes, scales, st)
+             : launch_quant_layout<false, kScalesTiled128>(x, T, d, slot_to_row, k, codes, scales, st);
 }
 
 }  // namespace

@@ -59,7 +59,8 @@ def _special_rows(d):
 
 
 @pytest.mark.parametrize("layout", [0, 1])
-@pytest.mark.parametrize("T,d", [(300, 3584), (8, 256), (1, 128)])
+@pytest.mark.parametrize("T,d", [(300, 3584), (8, 256), (1, 128),
+                                 (1000, 3584), (1500, 2048)])   # the last two: 16 inputs a thread
 def test_quant_mxfp4_dense_bit_exact(abi, orc, T, d, layout):
     x = torch.randn(T, d, generator=torch.Generator().manual_seed(T)).to(torch.bfloat16)
     codes, scales = _quant4_gpu(abi, x, layout=layout)
@@ -75,6 +76,14 @@ def test_quant_mxfp4_special_values_bit_exact(abi, orc):
     assert np.array_equal(scales[:9], rs)
     assert np.array_equal(codes[:9], rc)
     assert np.all(codes[1] == 0x88) and np.all(scales[0] == 0)
+
+
+def test_quant_mxfp4_special_values_large_batch_bit_exact(abi, orc):
+    x = _special_rows(4096).repeat(80, 1)    # 720 rows x 4096: 16 inputs a thread
+    codes, scales = _quant4_gpu(abi, x)
+    rc, rs = orc.mxfp4_quant_rows_bf16(synth.bf16_bits(x))
+    assert np.array_equal(scales[:720], rs)
+    assert np.array_equal(codes[:720], rc)
 
 
 @pytest.mark.parametrize("pad,layout", [(128, 0), (32, 1)])

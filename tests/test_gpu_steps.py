@@ -153,10 +153,11 @@ def test_permute_flags_bad_ids_on_device(abi):
     assert got["status"] == 6  # MOE_ERR_DEVICE_BAD_INPUT
 
 
-def _quant_gpu(abi, x_bf16, slot_to_row=None, k=0, rows_capacity=None, layout=0):
+def _quant_gpu(abi, x_bf16, slot_to_row=None, k=0, rows_capacity=None, layout=0, codes_offset=0):
     T, d = x_bf16.shape
     rc = rows_capacity or (T + 127) // 128 * 128
-    codes = torch.zeros(rc, d, dtype=torch.uint8, device="cuda")
+    codes = torch.zeros(rc * d + codes_offset, dtype=torch.uint8,
+                        device="cuda")[codes_offset:].view(rc, d)
     scales = torch.zeros(abi.moe_activation_scale_bytes(rc, d, layout), dtype=torch.uint8,
                          device="cuda")
     s2r = None if slot_to_row is None else torch.from_numpy(slot_to_row).cuda()
@@ -182,13 +183,32 @@ def _special_rows(d):
 
 
 @pytest.mark.parametrize("layout", [0, 1])
-@pytest.mark.parametrize("T,d", [(300, 3584), (8, 256), (1, 128)])
+@pytest.mark.parametrize("T,d", [(300, 3584), (8, 256), (1, 128),
+                                 (1000, 3584), (1500, 2048)])   # the last two: 16 inputs a thread
 def test_quant_dense_bit_exact(abi, orc, T, d, layout):
     x = torch.randn(T, d, generator=torch.Generator().manual_seed(T)).to(torch.bfloat16)
     codes, scales = _quant_gpu(abi, x, layout=layout)
     rc, rs = orc.mx_quant_rows_bf16(synth.bf16_bits(x))
     assert np.array_equal(codes[:T], rc)
     assert np.array_equal(scales[:T], rs)
+
+
+def test_quant_large_batch_codes_only_8_byte_aligned(abi, orc):
+    """A large batch into a code buffer 8 but not 16 bytes aligned takes the
+    8-inputs-a-thread kernel and gives the same bits."""
+    x = torch.randn(1000, 3584, generator=torch.Generator().manual_seed(12)).to(torch.bfloat16)
+    codes, scales = _quant_gpu(abi, x, codes_offset=8)
+    rc, rs = orc.mx_quant_rows_bf16(synth.bf16_bits(x))
+    assert np.array_equal(codes[:1000], rc)
+    assert np.array_equal(scales[:1000], rs)
+
+
+def test_quant_special_values_large_batch_bit_exact(abi, orc):
+    x = _special_rows(4096).repeat(90, 1)    # 720 rows x 4096: 16 inputs a thread
+    codes, scales = _quant_gpu(abi, x)
+    rc, rs = orc.mx_quant_rows_bf16(synth.bf16_bits(x))
+    assert np.array_equal(scales[:720], rs)
+    assert np.array_equal(codes[:720], rc)
 
 
 def test_quant_special_values_bit_exact(abi, orc):
