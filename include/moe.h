@@ -49,7 +49,9 @@
  *                          Groups padded to 128 rows; activation scales in
  *                          the TILED layout.
  *   MOE_GEMM_WEIGHT_TILES  weights are the M side (128 weight rows per MMA),
- *                          an expert's tokens the N side in chunks of 32; for
+ *                          an expert's tokens the N side in chunks of 32, or
+ *                          of 64 when rows_capacity exceeds 55 rows per
+ *                          expert (more than ~24 routed rows per expert); for
  *                          a few tokens per expert (decode), where streaming
  *                          the weights from HBM is the bound. Groups padded to
  *                          32 rows; activation scales in the GROUP32 layout.
@@ -154,11 +156,12 @@ int32_t moe_abi_version(void);
 size_t moe_tiled_scale_bytes(int64_t rows, int32_t K);
 
 /* The GEMM kernels moe_forward uses for MOE_GEMM_AUTO: MOE_GEMM_WEIGHT_TILES
- * while the experts average at most 28 routed rows (T*k <= 28*E), else
+ * while the experts average at most 56 routed rows (T*k <= 56*E), else
  * MOE_GEMM_TOKEN_TILES. On GB300 at the full layer dims the weight tiles
- * stream the weights at ~93% of HBM bandwidth up to T = 1536 tokens, while
- * the token tiles are bound by their 128-row tensor work below ~2048 tokens
- * and win above. Returns -1 for an unsupported shape. */
+ * stream the weights at 80-94% of HBM bandwidth up to T = 3072 tokens (32-
+ * then 64-token chunks), while the token tiles are bound by their 128-row
+ * tensor work there and win from T = 3584. Returns -1 for an unsupported
+ * shape. */
 int32_t moe_default_kernel(int32_t T, int32_t E, int32_t k);
 
 /* Bytes of an activation scale array for `rows` rows of K inputs in the given

@@ -61,11 +61,13 @@ cudaError_t launch_w2(int32_t kernel, const uint8_t* hq, const uint8_t* hs, cons
 // GB300 at full layer size, token tiles stream the weights faster than weight
 // tiles at every batch tried (64 and 512 tokens as well as prefill), so AUTO
 // picks token tiles for every shape.
-// Weight tiles (32-token chunks on the MMA's N side) while an expert holds few
-// tokens; token tiles (128-token tiles on M) once the 32-token chunks cost
-// more tensor work than the 128-row tiles waste on padding.
+// Weight tiles (32- or 64-token chunks on the MMA's N side) while the experts
+// average at most 56 routed rows; token tiles (128-token tiles on M) above,
+// where two 64-token chunks per expert cost more than the 128-row tiles
+// waste on padding (measured at the full dims: weight tiles ahead up to
+// T = 3072, token tiles from T = 3584).
 int32_t auto_kernel(int32_t T, int32_t E, int32_t k) {
-  return int64_t(T) * k <= 28 * int64_t(E) ? MOE_GEMM_WEIGHT_TILES : MOE_GEMM_TOKEN_TILES;
+  return int64_t(T) * k <= 56 * int64_t(E) ? MOE_GEMM_WEIGHT_TILES : MOE_GEMM_TOKEN_TILES;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -54,8 +54,8 @@ def test_size_helpers():
     assert abi.moe_rows_capacity(8, 32, 4, 128) == (32 + 32 * 127 + 127) // 128 * 128
     assert abi.moe_rows_capacity(8, 32, 4, 100) == -1    # not a power of two
     assert abi.moe_default_kernel(64, 896, 16) == abi.GEMM_WEIGHT_TILES
-    assert abi.moe_default_kernel(1568, 896, 16) == abi.GEMM_WEIGHT_TILES
-    assert abi.moe_default_kernel(1569, 896, 16) == abi.GEMM_TOKEN_TILES
+    assert abi.moe_default_kernel(3136, 896, 16) == abi.GEMM_WEIGHT_TILES
+    assert abi.moe_default_kernel(3137, 896, 16) == abi.GEMM_TOKEN_TILES
     assert abi.moe_default_kernel(8192, 896, 16) == abi.GEMM_TOKEN_TILES
     assert abi.moe_default_kernel(8, 896, 33) == -1
     assert abi.moe_permute_workspace_size(0, 896) == 256

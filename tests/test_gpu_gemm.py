@@ -3,8 +3,8 @@ oracle's per-expert stage functions, on ragged expert groups: empty groups,
 groups of 1, 15..17, 127..129 and several hundred rows, K not a multiple of the
 pipeline depth, and more tiles than SMs. All three kernel families: token
 tiles (tokens on the MMA's M side, groups padded to 128, TILED activation
-scales), weight tiles (weights on the M side, tokens as N = 32 per tile,
-groups padded to 32, GROUP32 activation scales) and pair tiles (weights on the
+scales), weight tiles (weights on the M side, tokens as N = 32 or 64 per
+tile by the groups' size, groups padded to 32, GROUP32 activation scales) and pair tiles (weights on the
 M side of a 2-CTA MMA, tokens as N in chunks of 128 / 256 with a ragged last
 chunk, groups padded to 128, TILED scales; d and I multiples of 256)."""
 import numpy as np
@@ -78,6 +78,9 @@ def _check_mxfp8_rows(got_c, got_s, ref_c, ref_s):
 
 
 CASES = [
+    # few tokens per expert: weight tiles in 32-token chunks (the larger
+    # groups below take 64-token chunks)
+    ([1, 0, 5, 31, 32, 33, 2, 17], 256, 384),
     ([0, 1, 15, 16, 17, 127, 128, 129, 300], 256, 256),
     ([3, 0, 250, 130, 33, 64, 96, 65], 384, 384),
     (list(np.random.default_rng(0).integers(0, 300, 40)), 256, 512),
