@@ -70,13 +70,14 @@ def test_host_pipeline_matches_forward(abi):
 
 
 @pytest.mark.parametrize("name,n,a4w4", [("decode_t64", 60, False), ("decode_t64", 30, True),
-                                         ("prefill_skewed_t8192", 10, False)])
+                                         ("prefill_skewed_t8192", 10, False),
+                                         ("uniform_t2048", 20, False)])   # 64-token chunks
 def test_repeated_forwards_bit_identical(abi, name, n, a4w4):
     """Back-to-back forwards, eager and replayed as a graph, give the first
     forward's output bit for bit. Consecutive kernels overlap through
     programmatic dependent launch; a missing wait would show up here as a
     difference between repetitions."""
-    wl = synth.workload(name)
+    wl = synth.full_dims(2048) if name == "uniform_t2048" else synth.workload(name)
     L = synth.make_layer(wl, seed=3, device="cuda")
     layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k)
     ws = layer.workspace(wl.T)
