@@ -160,7 +160,9 @@ def source_hash(paths):
 # Kernel source files per GEMM family: a committed traffic figure is only used
 # while these files are unchanged since its capture.
 FAMILY_SOURCES = {
-    "token_tiles": ["mxfp4_latent_moe_gb300/csrc/gemm.cu", "mxfp4_latent_moe_gb300/csrc/common.cuh"],
+    "token_tiles": ["mxfp4_latent_moe_gb300/csrc/gemm.cu",
+                    "mxfp4_latent_moe_gb300/csrc/gemm_token_pair.cu",
+                    "mxfp4_latent_moe_gb300/csrc/common.cuh"],
     "weight_tiles": ["mxfp4_latent_moe_gb300/csrc/gemm_decode.cu",
                      "mxfp4_latent_moe_gb300/csrc/common.cuh"],
     "pair_tiles": ["mxfp4_latent_moe_gb300/csrc/gemm_pair.cu",
@@ -547,8 +549,11 @@ def measure_layer(args, wl, dev, sampler, a4w4=False):
         raise RuntimeError("device status error in the timed forwards (%s)" % wl.name)
     # this library's kernels per forward: route, grouping (one kernel for a
     # one-chunk batch of T <= 256 tokens, else count + scan + scatter),
-    # quantisation, the two GEMMs, combine
-    launches_per_step = 6 if T <= 256 else 8
+    # quantisation, the two GEMMs, combine; a token-tile GEMM stage is two
+    # launches (the heavy experts' CTA pairs of m-tiles, then the rest)
+    token_stages = (2 if kernel == abi.GEMM_TOKEN_TILES else
+                    1 if a4w4 else 0)   # A4W4 stage 1 always runs token tiles
+    launches_per_step = (6 if T <= 256 else 8) + token_stages
 
     # ---- per-kernel breakdown: the same kernels through the step entry points
     rc = rows_cap

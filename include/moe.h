@@ -46,8 +46,13 @@
  * Two kernel families run the grouped GEMMs (moe_gemm_kernel):
  *   MOE_GEMM_TOKEN_TILES   tokens are the MMA's M side (128-row tiles),
  *                          weights the N side; for many tokens per expert.
- *                          Groups padded to 128 rows; activation scales in
- *                          the TILED layout.
+ *                          An expert with at least 8 tiles (more than 896
+ *                          tokens) runs its full pairs of tiles as one
+ *                          256-row MMA over a pair of SMs, in a launch
+ *                          before the one for the other tiles; the results
+ *                          are those of one tile at a time. Groups padded
+ *                          to 128 rows; activation scales in the TILED
+ *                          layout.
  *   MOE_GEMM_WEIGHT_TILES  weights are the M side (128 weight rows per MMA),
  *                          an expert's tokens the N side in chunks of 32, or
  *                          of 64 when rows_capacity exceeds 55 rows per

@@ -236,6 +236,27 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Token tiles of one expert (128 rows each, "m-tiles"): an expert with at
+// least this many runs its full pairs of m-tiles as CTA pairs (one 256-row
+// MMA over two SMs) and only an odd last one in the single-CTA kernel; a
+// lighter expert runs whole in the single-CTA kernel. With about five m-tiles
+// per expert (uniform routing at T = 32,768) nearly every expert has an odd
+// last tile, which then runs as a separate wave after the pairs.
+constexpr int kPairMinMtiles = 8;
+__device__ __forceinline__ bool runs_as_pairs(int mtiles) { return mtiles >= kPairMinMtiles; }
+
+// One 32-byte store (the address 32-byte aligned). A warp's 32 rows then
+// write whole 32-byte sectors; with 16-byte stores, which leave each sector
+// half written per request, the GEMM epilogues' stores cost the stage-2
+// kernel about 1.7 times as much time.
+__device__ __forceinline__ void st_global_32B(void* dst, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                              uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0),
+               "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMA / bulk copies (global -> shared, completion counted on an mbarrier)
 // ---------------------------------------------------------------------------
@@ -440,6 +461,13 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster with no memory ordering
+// (the arriving thread orders what it must by other means, e.g. completed
+// tensor-memory loads); a release at cluster scope costs far more latency.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 // try_wait with acquire at cluster scope (the phase may complete by arrivals

@@ -97,19 +97,8 @@ struct GemmParams {
   uint16_t* out_bf16;    // MODE 1: yp [rows][d]
   int* status;
   bool out32;            // the output base is 32-byte aligned: 32-byte stores
+  bool tail_only;        // only each expert's odd last m-tile (the others ran as CTA pairs)
 };
-
-// One 32-byte store (the address 32-byte aligned). A warp's 32 rows then
-// write whole 32-byte sectors; with 16-byte stores, which leave each sector
-// half written per request, the epilogue's stores cost the stage-2 kernel
-// about 1.7 times as much time.
-__device__ __forceinline__ void st_global_32B(void* dst, uint32_t a0, uint32_t a1, uint32_t a2,
-                                              uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
-                                              uint32_t a7) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0),
-               "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
-               : "memory");
-}
 
 // ---- 2-CTA clusters: the A tile multicast to both CTAs of a pair ----------
 // TMA load delivered to the same shared-memory offset (and mbarrier) in every
@@ -131,10 +120,23 @@ __device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
       : "memory");
 }
 
-// Tile -> (expert, n-tile, first row). An expert's m-tiles cover its tokens
-// (ceil(counts[e]/BM) of them); the m-tile index runs fastest.
+// m-tiles of an expert this launch covers: all ceil(count/BM), or with
+// tail_only, for an expert that runs as CTA pairs, the last one when their
+// number is odd (the full pairs before it run in the CTA-pair kernel).
+__device__ __forceinline__ int expert_mtiles(int count, bool tail_only) {
+  const int m = (count + BM - 1) / BM;
+  return tail_only && runs_as_pairs(m) ? (m & 1) : m;
+}
+// The first m-tile of the expert that this launch covers.
+__device__ __forceinline__ int expert_first_mtile(int count, bool tail_only) {
+  const int m = (count + BM - 1) / BM;
+  return tail_only && runs_as_pairs(m) ? m - 1 : 0;
+}
+
+// Tile -> (expert, n-tile, first row); the m-tile index runs fastest.
 __device__ __forceinline__ void decode_tile(int tile, const int* prefix, const int* offs,
-                                            const int* cnts, int E, int& e, int& nt, int& row0) {
+                                            const int* cnts, int E, bool tail_only, int& e,
+                                            int& nt, int& row0) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -143,9 +145,9 @@ __device__ __forceinline__ void decode_tile(int tile, const int* prefix, const i
   }
   e = lo;
   const int r = tile - prefix[e];
-  const int mtiles = (cnts[e] + BM - 1) / BM;
+  const int mtiles = expert_mtiles(cnts[e], tail_only);
   nt = r / mtiles;
-  row0 = offs[e] + (r - nt * mtiles) * BM;
+  row0 = offs[e] + (expert_first_mtile(cnts[e], tail_only) + r - nt * mtiles) * BM;
 }
 
 // MODE 0: w13 + GLU + MXFP8 requant of h (scales of h in layout HSL);
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = e0; e < e1; ++e) {
       const int rows = offs[e + 1] - offs[e];
       bad |= rows < 0 || rows % BM != 0 || cnts[e] < 0 || cnts[e] > rows;
-      s += max(0, (cnts[e] + BM - 1) / BM) * ntu;
+      s += max(0, expert_mtiles(cnts[e], p.tail_only)) * ntu;
     }
     bad = __any_sync(0xffffffffu, bad);
     int incl = s;
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = incl - s;
     for (int e = e0; e < e1; ++e) {
       prefix[e] = run;
-      run += max(0, (cnts[e] + BM - 1) / BM) * ntu;
+      run += max(0, expert_mtiles(cnts[e], p.tail_only)) * ntu;
     }
     if (lane == 31) {
       const bool ok = !bad && offs[0] == 0 && int64_t(offs[E]) <= p.rows_capacity;
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool failed = false;
     for (int unit = unit0; unit < total && !failed; unit += units_step) {
       int e, nu, row0;
-      decode_tile(unit, prefix, offs, cnts, E, e, nu, row0);
+      decode_tile(unit, prefix, offs, cnts, E, p.tail_only, e, nu, row0);
       const int nt = nu * CL + int(crank);
       const bool dummy = CL == 2 && nt >= p.n_tiles;   // pair partner without an n-tile
       for (int kt = 0; kt < KT; ++kt) {
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool dummy = false;
       if (CL == 2 && crank == 1 && (p.n_tiles & 1)) {
         int e, nu, row0;
-        decode_tile(unit, prefix, offs, cnts, E, e, nu, row0);
+        decode_tile(unit, prefix, offs, cnts, E, p.tail_only, e, nu, row0);
         dummy = nu * CL + int(crank) >= p.n_tiles;
       }
       if (!mbar_wait_warp(acc_empty, acc_phase ^ 1u, abort_flag)) {
@@ -462,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int unit = unit0; unit < total; unit += units_step) {
       int e, nu, row0;
-      decode_tile(unit, prefix, offs, cnts, E, e, nu, row0);
+      decode_tile(unit, prefix, offs, cnts, E, p.tail_only, e, nu, row0);
       const int nt = nu * CL + int(crank);
       const bool dummy = CL == 2 && nt >= p.n_tiles;   // warp-uniform
       bool ok = mbar_wait(acc_full, acc_phase, abort_flag);
@@ -713,10 +715,16 @@ int sm_count() {
   return n;
 }
 
+// The token-tile family: the full pairs of m-tiles of the experts with at
+// least kPairMinMtiles of them as CTA pairs (gemm_token_pair.cu), then the
+// rest here, one CTA per m-tile.
 cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,
                                 const int* offsets, int E, int d, int I, const uint8_t* w13,
                                 const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
                                 int64_t rows_capacity, int* status, cudaStream_t st) {
+  cudaError_t err = launch_token_pairs_w13_glu(xq, xs, counts, offsets, E, d, I, w13, w13_sf, hq,
+                                               hs, rows_capacity, status, st);
+  if (err != cudaSuccess) return err;
   CUtensorMap ta, tb;
   if (!encode_operand(&ta, xq, false, d, rows_capacity, BM / kPairCL))
     return cudaErrorInvalidValue;
@@ -736,6 +744,7 @@ cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int*
   p.out_sf = hs;
   p.status = status;
   p.out32 = (reinterpret_cast<uintptr_t>(hq) & 31u) == 0;
+  p.tail_only = true;
   return launch_mode<0>(p, ta, tb, st);
 }
 
@@ -744,6 +753,9 @@ cudaError_t launch_gemm_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs, const
                                      const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
                                      int hs_layout, int64_t rows_capacity, int* status,
                                      cudaStream_t st) {
+  cudaError_t err = launch_token_pairs_w13_glu_a4w4(xq, xs, counts, offsets, E, d, I, w13, w13_sf,
+                                                    hq, hs, hs_layout, rows_capacity, status, st);
+  if (err != cudaSuccess) return err;
   CUtensorMap ta, tb;
   // packed activations: d/2 bytes per row, 128-byte boxes of 128 rows
   if (!encode_operand(&ta, xq, false, d / 2, rows_capacity, BM / kPairCL))
@@ -764,6 +776,7 @@ cudaError_t launch_gemm_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs, const
   p.out_sf = hs;
   p.status = status;
   p.out32 = (reinterpret_cast<uintptr_t>(hq) & 31u) == 0;
+  p.tail_only = true;
   if (hs_layout == kScalesGroup32) return launch_mode<0, true, kScalesGroup32>(p, ta, tb, st);
   return launch_mode<0, true, kScalesTiled128>(p, ta, tb, st);
 }
@@ -772,6 +785,9 @@ cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* coun
                            const int* offsets, int E, int I, int d, const uint8_t* w2,
                            const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity, int* status,
                            cudaStream_t st) {
+  cudaError_t err = launch_token_pairs_w2(hq, hs, counts, offsets, E, I, d, w2, w2_sf, yp,
+                                          rows_capacity, status, st);
+  if (err != cudaSuccess) return err;
   CUtensorMap ta, tb;
   if (!encode_operand(&ta, hq, false, I, rows_capacity, BM / kPairCL))
     return cudaErrorInvalidValue;
@@ -790,6 +806,7 @@ cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* coun
   p.out_bf16 = yp;
   p.status = status;
   p.out32 = (reinterpret_cast<uintptr_t>(yp) & 31u) == 0;
+  p.tail_only = true;
   return launch_mode<1>(p, ta, tb, st);
 }
 

@@ -54,6 +54,21 @@ cudaError_t launch_gemm_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs, const
                                      const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
                                      int hs_layout, int64_t rows_capacity, int* status,
                                      cudaStream_t st);
+// The full 256-row pairs of each expert's m-tiles over CTA pairs
+// (gemm_token_pair.cu); the launch_gemm_* entry points run these first.
+cudaError_t launch_token_pairs_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,
+                                       const int* offsets, int E, int d, int I, const uint8_t* w13,
+                                       const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,
+                                       int64_t rows_capacity, int* status, cudaStream_t st);
+cudaError_t launch_token_pairs_w13_glu_a4w4(const uint8_t* xq, const uint8_t* xs,
+                                            const int* counts, const int* offsets, int E, int d,
+                                            int I, const uint8_t* w13, const uint8_t* w13_sf,
+                                            uint8_t* hq, uint8_t* hs, int hs_layout,
+                                            int64_t rows_capacity, int* status, cudaStream_t st);
+cudaError_t launch_token_pairs_w2(const uint8_t* hq, const uint8_t* hs, const int* counts,
+                                  const int* offsets, int E, int I, int d, const uint8_t* w2,
+                                  const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity,
+                                  int* status, cudaStream_t st);
 cudaError_t launch_gemm_w2(const uint8_t* hq, const uint8_t* hs, const int* counts,
                            const int* offsets, int E, int I, int d, const uint8_t* w2,
                            const uint8_t* w2_sf, uint16_t* yp, int64_t rows_capacity, int* status,
@@ -69,6 +84,7 @@ EncodeTiledFn encode_tiled_fn();   // cuTensorMapEncodeTiled through the runtime
 bool encode_operand(CUtensorMap* map, const void* base, bool e2m1, int K, int64_t rows,
                     int box_rows);
 bool encode_boxed_weights(CUtensorMap* map, const void* base, int64_t rows, int K);
+bool encode_boxed_weights_packed(CUtensorMap* map, const void* base, int64_t rows, int K);
 // A TILED scale array as rows of 128 bytes, boxes of one 512-byte atom.
 bool encode_scale_atoms(CUtensorMap* map, const void* base, int64_t bytes);
 int sm_count();
