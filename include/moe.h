@@ -46,11 +46,12 @@
  * Two kernel families run the grouped GEMMs (moe_gemm_kernel):
  *   MOE_GEMM_TOKEN_TILES   tokens are the MMA's M side (128-row tiles),
  *                          weights the N side; for many tokens per expert.
- *                          An expert with at least 8 tiles (more than 896
- *                          tokens) runs its full pairs of tiles as one
- *                          256-row MMA over a pair of SMs, in a launch
- *                          before the one for the other tiles; the results
- *                          are those of one tile at a time. Groups padded
+ *                          An expert with an even number of tiles, or with
+ *                          at least 8 (more than 896 tokens), runs its full
+ *                          pairs of tiles as one 256-row MMA over a pair of
+ *                          SMs, in a launch before the one for the other
+ *                          tiles; the results are those of one tile at a
+ *                          time. Groups padded
  *                          to 128 rows; activation scales in the TILED
  *                          layout.
  *   MOE_GEMM_WEIGHT_TILES  weights are the M side (128 weight rows per MMA),

@@ -236,14 +236,17 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Token tiles of one expert (128 rows each, "m-tiles"): an expert with at
-// least this many runs its full pairs of m-tiles as CTA pairs (one 256-row
-// MMA over two SMs) and only an odd last one in the single-CTA kernel; a
-// lighter expert runs whole in the single-CTA kernel. With about five m-tiles
-// per expert (uniform routing at T = 32,768) nearly every expert has an odd
-// last tile, which then runs as a separate wave after the pairs.
+// Token tiles of one expert (128 rows each, "m-tiles"): an expert with an
+// even number of them, or with at least kPairMinMtiles, runs its full pairs
+// of m-tiles as CTA pairs (one 256-row MMA over two SMs) and only an odd last
+// one in the single-CTA kernel; any other expert (1, 3, 5 or 7 m-tiles) runs
+// whole in the single-CTA kernel. An odd last m-tile runs in a second launch
+// that streams the expert's weights again: with five m-tiles per expert
+// (uniform routing at T = 32,768) that cost more than the pairs saved.
 constexpr int kPairMinMtiles = 8;
-__device__ __forceinline__ bool runs_as_pairs(int mtiles) { return mtiles >= kPairMinMtiles; }
+__device__ __forceinline__ bool runs_as_pairs(int mtiles) {
+  return mtiles >= kPairMinMtiles || (mtiles >= 2 && (mtiles & 1) == 0);
+}
 
 // One 32-byte store (the address 32-byte aligned). A warp's 32 rows then
 // write whole 32-byte sectors; with 16-byte stores, which leave each sector

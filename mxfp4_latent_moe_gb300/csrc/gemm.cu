@@ -715,9 +715,9 @@ int sm_count() {
   return n;
 }
 
-// The token-tile family: the full pairs of m-tiles of the experts with at
-// least kPairMinMtiles of them as CTA pairs (gemm_token_pair.cu), then the
-// rest here, one CTA per m-tile.
+// The token-tile family: the full pairs of m-tiles of the experts that run
+// as pairs (runs_as_pairs) on CTA pairs (gemm_token_pair.cu), then the rest
+// here, one CTA per m-tile.
 cudaError_t launch_gemm_w13_glu(const uint8_t* xq, const uint8_t* xs, const int* counts,
                                 const int* offsets, int E, int d, int I, const uint8_t* w13,
                                 const uint8_t* w13_sf, uint8_t* hq, uint8_t* hs,

@@ -1,6 +1,6 @@
 // Grouped GEMMs of the routed experts over CTA pairs: the prefill path for
-// the full 256-row pairs of 128-row m-tiles of the experts that hold at least
-// kPairMinMtiles m-tiles (the heavy experts of a skewed routing).
+// the full 256-row pairs of 128-row m-tiles of the experts that hold an even
+// number of m-tiles or at least kPairMinMtiles of them (runs_as_pairs).
 //
 // Same arithmetic as the single-CTA token tiles (gemm.cu; "Kimi K3.1 Pro on
 // AMD Instinct GPUs" and "The MXFP4 latent MoE on FlyDSL" for the MXFP4
@@ -17,13 +17,13 @@
 // six stages fit in shared memory instead of four. With four, a stage's slot
 // is held for its copies' latency plus the MMA's completion (about 2,600
 // cycles at full load), which caps the tensor pipe near 75%; six cover it.
-// Such an expert's odd last m-tile has no partner and runs in the single-CTA
-// kernel, launched after this one, with every m-tile of the lighter experts.
-// With few m-tiles per expert the odd last tiles are a large share of the
-// work and run as an extra wave after the pairs: measured on the uniform
-// routing at T = 32,768 (five m-tiles per expert), pairs for every expert
-// made the layer about 3% slower, while at the skewed T = 8,192 pairs for the
-// heavy experts made it 2% (MXFP8) to 5% (A4W4) faster.
+// A heavy expert's odd last m-tile has no partner and runs in the single-CTA
+// kernel, launched after this one, with every m-tile of the experts that do
+// not run as pairs. Measured on the full layer: with 2 or 4 m-tiles per
+// expert (uniform routing at T = 8,192 and 24,576) pairs made it 7-9%
+// (MXFP8) and 11-12% (A4W4) faster, at the skewed T = 8,192 (heavy experts)
+// 2% and 5%; with five per expert (T = 32,768), pairs plus a second launch
+// for every expert's odd last m-tile made it 3% slower.
 //
 // CTA organisation: 2-CTA clusters, persistent, 320 threads per CTA.
 //   warp 0      TMA producer in both CTAs: its 128 token rows, its 128 weight

@@ -52,9 +52,14 @@ WORKLOADS = [
 ]
 # Reduced cases of the same kernels for profiler captures (about 1 GB of
 # weights, still far larger than the 129 MB L2): full d and I, 64 experts.
+# At T = 1792 every expert holds 4 token tiles of 128 rows (448 routed rows
+# on average, standard deviation 18), at T = 2304 five (576 on average, 21),
+# as at T = 32,768 with 896 experts.
 PROFILE_WORKLOADS = [
     Workload("ncu_decode_t64_e64", T=64, d=3584, E=64, k=16, I=3072),
     Workload("ncu_prefill_t2048_e64", T=2048, d=3584, E=64, k=16, I=3072),
+    Workload("ncu_prefill_t1792_e64", T=1792, d=3584, E=64, k=16, I=3072),
+    Workload("ncu_prefill_t2304_e64", T=2304, d=3584, E=64, k=16, I=3072),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS}
 

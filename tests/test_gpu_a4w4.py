@@ -106,9 +106,11 @@ CASES = [
     ([0, 1, 15, 16, 17, 127, 128, 129, 300], 256, 256),
     ([3, 0, 250, 130, 33, 64, 96, 65], 512, 384),
     (list(np.random.default_rng(0).integers(0, 300, 40)), 256, 512),
-    # experts of at least 8 m-tiles as CTA pairs of m-tiles (odd and even
-    # m-tile counts, 1- and 20-row last tiles), one just below
+    # CTA pairs of m-tiles (even counts, and odd ones of at least 8, with 1-
+    # and 20-row last tiles) beside single-CTA experts (7 m-tiles)
     ([1100, 0, 1024, 896, 897, 129, 1300], 256, 256),
+    # every expert with an even m-tile count: all CTA pairs, no single-CTA work
+    ([256, 200, 512, 129, 0], 256, 256),
 ]
 
 
@@ -163,7 +165,8 @@ def _host_layer(L):
     synth.shape("skewed", T=300, d=256, E=64, k=8, I=256, skew=True),
     synth.shape("outliers", T=100, d=512, E=16, k=4, I=128, outlier_frac=0.05),
     synth.shape("one_expert", T=130, d=256, E=1, k=1, I=256),
-    # the top-ranked experts hold 8 or more m-tiles: CTA pairs of m-tiles
+    # the top-ranked experts hold 8 or more m-tiles (CTA pairs of m-tiles and
+    # an odd last one on a single CTA)
     synth.shape("heavy_experts", T=1500, d=256, E=16, k=4, I=256, skew=True),
 ])
 @pytest.mark.parametrize("kernel", [1, 2, 3])

@@ -46,7 +46,8 @@ def _host_layer(L):
     synth.shape("outliers", T=100, d=384, E=16, k=4, I=128, outlier_frac=0.05),
     synth.shape("one_expert", T=130, d=256, E=1, k=1, I=256),
     synth.shape("all_experts", T=20, d=128, E=8, k=8, I=128),
-    # the top-ranked experts hold 8 or more m-tiles: CTA pairs of m-tiles
+    # the top-ranked experts hold 8 or more m-tiles (CTA pairs of m-tiles and
+    # an odd last one on a single CTA)
     synth.shape("heavy_experts", T=1500, d=256, E=16, k=4, I=256, skew=True),
 ])
 @pytest.mark.parametrize("kernel", [1, 2])

@@ -3,7 +3,8 @@ oracle's per-expert stage functions, on ragged expert groups: empty groups,
 groups of 1, 15..17, 127..129 and several hundred rows, K not a multiple of the
 pipeline depth, and more tiles than SMs. All three kernel families: token
 tiles (tokens on the MMA's M side, groups padded to 128, TILED activation
-scales; experts of at least 8 m-tiles as 2-CTA pairs of m-tiles), weight tiles (weights on the M side, tokens as N = 32 or 64 per
+scales; experts with an even number of m-tiles or at least 8 as 2-CTA
+pairs of m-tiles), weight tiles (weights on the M side, tokens as N = 32 or 64 per
 tile by the groups' size, groups padded to 32, GROUP32 activation scales) and pair tiles (weights on the
 M side of a 2-CTA MMA, tokens as N in chunks of 128 / 256 with a ragged last
 chunk, groups padded to 128, TILED scales; d and I multiples of 256)."""
@@ -86,11 +87,14 @@ CASES = [
     (list(np.random.default_rng(0).integers(0, 300, 40)), 256, 512),
     # several token chunks per expert for the pair tiles (128 / 256 wide)
     ([0, 255, 256, 257, 1, 600, 383, 384, 31], 512, 512),
-    # token tiles: experts with at least 8 m-tiles of 128 rows run their full
-    # pairs of m-tiles over CTA pairs, the rest one CTA per m-tile: 9 m-tiles
-    # (odd, the last with 76 rows), 8 (even, full), 7 (below the threshold),
-    # 8 with a 1-row last tile, 11 with a 20-row last tile
+    # token tiles: experts with an even number of m-tiles of 128 rows, or at
+    # least 8, run their full pairs of m-tiles over CTA pairs, the rest one
+    # CTA per m-tile: 9 m-tiles (odd, the last with 76 rows), 8 (even, full),
+    # 7 (odd, below 8: single CTAs), 8 with a 1-row last tile, 2 with a
+    # 1-row last tile, 11 with a 20-row last tile
     ([1100, 0, 1024, 896, 897, 129, 1300], 256, 256),
+    # every expert with an even m-tile count: all CTA pairs, no single-CTA work
+    ([256, 200, 512, 129, 0], 256, 256),
 ]
 
 
