@@ -182,15 +182,26 @@ def test_forward_a4w4_small_all_outputs(abi, orc, wl, kernel):
     gu.assert_layer_close(gu.bf16_to_f64(y), ref["y64"])
 
 
-@pytest.mark.parametrize("name", ["decode_t64", "prefill_skewed_t8192"])
+@pytest.mark.parametrize("name", ["decode_t64", "prefill_skewed_t8192", "prefill_outlier_t32768",
+                                  "uniform_t8192"])
 def test_forward_a4w4_full_size_sampled(abi, orc, name):
-    wl = synth.workload(name)
+    """Routing on every token; the output on 128 seeded tokens plus, at
+    T = 32,768, every outlier token (rows scaled by 64). uniform_t8192: most
+    experts hold 2 m-tiles, so stage 1 runs mostly as CTA pairs."""
+    wl = (synth.full_dims(int(name[len("uniform_t"):])) if name.startswith("uniform_t")
+          else synth.workload(name))
     L = synth.make_layer(wl, seed=0, device="cuda")
     y, ids, _ = _run_a4w4(abi, wl, L)
     logits = L["logits"].cpu().numpy()
     rids, _ = orc.route_topk(logits, wl.k)
     assert np.array_equal(ids.cpu().numpy(), rids)
-    tok = np.sort(np.random.default_rng(77).choice(wl.T, size=16, replace=False))
+    tok = set(np.random.default_rng(77).choice(wl.T, size=min(128, wl.T), replace=False).tolist())
+    if wl.outlier_frac > 0:
+        amax = L["x"].float().abs().amax(dim=1).cpu().numpy()
+        out = np.nonzero(amax > 32.0)[0]    # N(0,1) rows stay far below; x64 rows far above
+        assert len(out) == int(round(wl.outlier_frac * wl.T))
+        tok |= set(out.tolist())
+    tok = np.array(sorted(tok))
     H = _host_layer(L)
     ref = orc.moe_forward(synth.bf16_bits(L["x"][torch.from_numpy(tok).cuda()]), logits[tok],
                           wl.k, H["w13"], H["w13_s"], H["w2"], H["w2_s"], want_y64=True,

@@ -107,7 +107,8 @@ def _workload_state(orc, name):
         return _CACHE[name]
     _CACHE.clear()
     torch.cuda.empty_cache()
-    wl = synth.workload(name)
+    wl = (synth.full_dims(int(name[len("uniform_t"):])) if name.startswith("uniform_t")
+          else synth.workload(name))
     L = synth.make_layer(wl, seed=0, device="cuda")
     tok = _compared_tokens(wl, L)
     xb = synth.bf16_bits(L["x"])
@@ -157,7 +158,10 @@ def _compared_tokens(wl, L):
                                          ("prefill_outlier_t32768", 0),
                                          ("prefill_outlier_t32768", 2),
                                          ("prefill_outlier_t32768", 1),
-                                         ("prefill_outlier_t32768", 3)])
+                                         ("prefill_outlier_t32768", 3),
+                                         # uniform routing at the full dims, 2 m-tiles for
+                                         # most experts: token tiles mostly as CTA pairs
+                                         ("uniform_t8192", 0)])
 def test_forward_full_size_workloads(abi, orc, name, kernel):
     """The benchmark's configuration (kernel family 0 = moe_default_kernel:
     weight tiles at decode, token tiles at prefill), and each workload through
