@@ -90,10 +90,20 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int* __restrict__ hi
   const int e = threadIdx.x;
   int cnt = 0;
   if (e < E) {
-    for (int c = 0; c < C; ++c) {  // exclusive prefix over chunks, in place
-      const int v = hist[int64_t(c) * E + e];
-      hist[int64_t(c) * E + e] = cnt;
-      cnt += v;
+    // exclusive prefix over chunks, in place; 16 chunks' counts are loaded
+    // before any of them is overwritten, so their loads are in flight
+    // together instead of one memory latency per chunk
+    constexpr int kBatch = 16;
+    for (int c0 = 0; c0 < C; c0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        v[i] = c0 + i < C ? hist[int64_t(c0 + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (c0 + i < C) hist[int64_t(c0 + i) * E + e] = cnt;
+        cnt += v[i];
+      }
     }
     counts[e] = cnt;
   }
