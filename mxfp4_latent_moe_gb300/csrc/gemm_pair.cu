@@ -42,9 +42,11 @@
 //               the stage in both CTAs with one multicast commit.
 //   warps 2-9   epilogue in both CTAs on their own 128 weight rows: tcgen05.ld
 //               of the accumulator, release (rank 1's warps arrive remotely on
-//               rank 0's accumulator-empty barrier), then the GLU + MX requant
-//               (MODE 0) or the bf16 conversion (MODE 1) while the next tile
-//               accumulates.
+//               rank 0's accumulator-empty barrier, relaxed: their tensor-memory
+//               reads have completed by tcgen05.wait::ld, and a release at
+//               cluster scope costs far more latency per tile), then the GLU +
+//               MX requant (MODE 0) or the bf16 conversion (MODE 1) while the
+//               next tile accumulates.
 // A first version announced the second CTA's landed stages to rank 0 through
 // a relay warp (cluster-scope release and acquire per stage) and ran 2.3x
 // slower than the single-CTA token tiles; completing the TMA bytes directly
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           if (rank == 0) mbar_arrive(acc_empty);
-          else mbar_arrive_remote(acc_empty_pair);
+          else mbar_arrive_remote_relaxed(acc_empty_pair);
         }
         acc_phase ^= 1u;
         // h of weight row i (this lane) for each token column; its MX block of
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           if (rank == 0) mbar_arrive(acc_empty);
-          else mbar_arrive_remote(acc_empty_pair);
+          else mbar_arrive_remote_relaxed(acc_empty_pair);
         }
         acc_phase ^= 1u;
         const int j = wt * PM + int(rank) * 128 + q * 32 + lane;   // output feature
