@@ -35,6 +35,14 @@
 // one (expert, m-tile), each CTA loads one 64-row half of the A tile and
 // multicasts it to both, so the activations cross from L2 once per pair
 // (on prefill about 10% faster stage 1 and 3-5% faster stage 2).
+// In the token-tile family this kernel runs the m-tiles of the experts with
+// 1, 3, 5 or 7 of them and the odd last m-tile of the heavier odd ones
+// (`tail_only`); every other full pair of m-tiles runs before it as one
+// 256-row MMA over two SMs (gemm_token_pair.cu). A stage here writes 49.5 KB
+// of shared memory per 512 cycles of MMA work, near the SM's TMA ingest
+// rate, so four stages cover the copies' latency only in part (the tensor
+// pipe runs about three quarters busy); the pair's stages need two thirds of
+// that.
 // Every wait is bounded; on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT,
 // drains its outstanding copies and tensor-core work, frees tensor memory and
 // exits.
