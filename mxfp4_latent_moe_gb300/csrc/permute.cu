@@ -65,10 +65,15 @@ __device__ __forceinline__ void build_masks(const int* __restrict__ ids, int T, 
   __syncthreads();
 }
 
+// Also sets this chunk's share of row_to_slot (ceil(rows / C) rows per
+// block) to -1, after griddepcontrol.wait (inside build_masks): the scatter,
+// two launches later, fills the used rows.
 __global__ void __launch_bounds__(kChunk) permute_count_kernel(const int* __restrict__ ids,
                                                                int T, int E, int k,
                                                                int* __restrict__ hist,
-                                                               int* status) {
+                                                               int* status,
+                                                               int* __restrict__ row_to_slot,
+                                                               int64_t rows_capacity) {
   extern __shared__ uint32_t masks[];
   pdl_trigger();
   build_masks(ids, T, E, k, masks, status);
@@ -77,6 +82,12 @@ __global__ void __launch_bounds__(kChunk) permute_count_kernel(const int* __rest
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) s += __popc(masks[w * E + e]);
     hist[int64_t(blockIdx.x) * E + e] = s;
+  }
+  if (row_to_slot) {
+    const int64_t per = (rows_capacity + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = min(rows_capacity, int64_t(blockIdx.x) * per);
+    const int64_t r1 = min(rows_capacity, r0 + per);
+    for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) row_to_slot[r] = -1;
   }
 }
 
@@ -275,23 +286,26 @@ cudaError_t launch_permute(const int* ids, int T, int E, int k, int pad_m, int* 
                       smem + size_t(E + 1) * sizeof(int), st, 1, ids, T, E, k, pad_m, counts,
                       offsets, slot_to_row, row_to_slot, rows_capacity, status);
   }
-  if (C > 0 && k > 0) {
-    const cudaError_t err = launch_ex(false, permute_count_kernel, dim3(C), dim3(kChunk), smem,
-                                      st, 1, ids, T, E, k, hist, status);
+  // Count, scan and scatter chain by programmatic dependent launch: each
+  // touches global memory only after griddepcontrol.wait, and the count
+  // kernel also resets row_to_slot.
+  const bool work = C > 0 && k > 0;
+  if (work) {
+    const cudaError_t err = launch_ex(true, permute_count_kernel, dim3(C), dim3(kChunk), smem,
+                                      st, 1, ids, T, E, k, hist, status, row_to_slot,
+                                      rows_capacity);
     if (err != cudaSuccess) return err;
   }
-  cudaError_t err = launch_ex(false, permute_scan_kernel, dim3(1), dim3(1024), 0, st, 1, hist,
-                              (k > 0) ? C : 0, E, pad_m, counts, offsets);
+  cudaError_t err = launch_ex(work, permute_scan_kernel, dim3(1), dim3(1024), 0, st, 1, hist,
+                              work ? C : 0, E, pad_m, counts, offsets);
   if (err != cudaSuccess) return err;
-  if (rows_capacity > 0 && row_to_slot) {
+  if (!work && rows_capacity > 0 && row_to_slot) {   // no count kernel to reset it
     err = cudaMemsetAsync(row_to_slot, 0xFF, size_t(rows_capacity) * sizeof(int), st);
     if (err != cudaSuccess) return err;
   }
-  if (C > 0 && k > 0) {
-    permute_scatter_kernel<<<C, kChunk, smem, st>>>(ids, T, E, k, hist, offsets, slot_to_row,
-                                                    row_to_slot, status);
-    err = cudaGetLastError();
-  }
+  if (work)
+    err = launch_ex(true, permute_scatter_kernel, dim3(C), dim3(kChunk), smem, st, 1, ids, T, E,
+                    k, hist, offsets, slot_to_row, row_to_slot, status);
   return err;
 }
 
