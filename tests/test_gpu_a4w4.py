@@ -168,6 +168,8 @@ def _host_layer(L):
     # the top-ranked experts hold 8 or more m-tiles (CTA pairs of m-tiles and
     # an odd last one on a single CTA)
     synth.shape("heavy_experts", T=1500, d=256, E=16, k=4, I=256, skew=True),
+    # 4 or 5 m-tiles per expert: stage 1 mostly as CTA pairs of m-tiles
+    synth.shape("even_mtiles", T=2048, d=256, E=8, k=2, I=256),
 ])
 @pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_forward_a4w4_small_all_outputs(abi, orc, wl, kernel):

@@ -49,6 +49,11 @@ def _host_layer(L):
     # the top-ranked experts hold 8 or more m-tiles (CTA pairs of m-tiles and
     # an odd last one on a single CTA)
     synth.shape("heavy_experts", T=1500, d=256, E=16, k=4, I=256, skew=True),
+    # the largest expert count and top-k the library accepts
+    synth.shape("max_e_max_k", T=64, d=128, E=1024, k=32, I=128),
+    # about 512 tokens for each of 8 experts: 4 (or 5) m-tiles each, token
+    # tiles mostly as CTA pairs
+    synth.shape("even_mtiles", T=2048, d=256, E=8, k=2, I=256),
 ])
 @pytest.mark.parametrize("kernel", [1, 2])
 def test_forward_small_all_outputs(abi, orc, wl, kernel):
