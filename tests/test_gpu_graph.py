@@ -1,7 +1,8 @@
 """The layer step captured as one CUDA graph (MoeLayer.capture): replays on
 refilled input buffers give bit-for-bit the eager moe_forward /
 moe_forward_a4w4 results (every kernel of the step is deterministic), for
-both GEMM families, with the device status clean after each replay."""
+both GEMM families (token tiles also with CTA pairs of m-tiles), with the
+device status clean after each replay."""
 import pytest
 import torch
 
@@ -22,6 +23,8 @@ def abi():
     (synth.shape("small", T=40, d=512, E=24, k=4, I=384), 0),
     (synth.shape("small", T=40, d=512, E=24, k=4, I=384), 1),
     (synth.workload("decode_t64"), 0),
+    # 4-5 m-tiles per expert: token tiles mostly as CTA pairs of m-tiles
+    (synth.shape("even_mtiles", T=2048, d=256, E=8, k=2, I=256), 1),
 ])
 def test_graph_replay_matches_eager(abi, wl, kernel, a4w4):
     L = synth.make_layer(wl, seed=0, device="cuda")
@@ -71,13 +74,15 @@ def test_host_pipeline_matches_forward(abi):
 
 @pytest.mark.parametrize("name,n,a4w4", [("decode_t64", 60, False), ("decode_t64", 30, True),
                                          ("prefill_skewed_t8192", 10, False),
-                                         ("uniform_t2048", 20, False)])   # 64-token chunks
+                                         ("uniform_t2048", 20, False),    # 64-token chunks
+                                         ("uniform_t12288", 10, False)])  # all CTA pairs
 def test_repeated_forwards_bit_identical(abi, name, n, a4w4):
     """Back-to-back forwards, eager and replayed as a graph, give the first
     forward's output bit for bit. Consecutive kernels overlap through
     programmatic dependent launch; a missing wait would show up here as a
     difference between repetitions."""
-    wl = synth.full_dims(2048) if name == "uniform_t2048" else synth.workload(name)
+    wl = (synth.full_dims(int(name[len("uniform_t"):])) if name.startswith("uniform_t")
+          else synth.workload(name))
     L = synth.make_layer(wl, seed=3, device="cuda")
     layer = MoeLayer(L["w13"], L["w13_s"], L["w2"], L["w2_s"], k=wl.k)
     ws = layer.workspace(wl.T)
