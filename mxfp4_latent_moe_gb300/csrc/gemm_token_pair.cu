@@ -126,7 +126,7 @@ __device__ __forceinline__ int full_pairs(int count) {
 
 // Unit -> (expert, n-tile, first row of the pair); the pair index runs fastest.
 __device__ __forceinline__ void pair_unit(int tile, const int* prefix, const int* offs,
-                                            const int* cnts, int E, int& e, int& nt, int& row0) {
+                                          const int* cnts, int E, int& e, int& nt, int& row0) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -148,9 +148,9 @@ __device__ __forceinline__ void pair_unit(int tile, const int* prefix, const int
 template <int MODE, bool A4, int HSL>
 __global__ void __launch_bounds__(kThreads, 1)
     token_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                        const __grid_constant__ CUtensorMap tmap_b,
-                        const __grid_constant__ CUtensorMap tmap_asf,
-                        const __grid_constant__ CUtensorMap tmap_bsf, const PairParams p) {
+                           const __grid_constant__ CUtensorMap tmap_b,
+                           const __grid_constant__ CUtensorMap tmap_asf,
+                           const __grid_constant__ CUtensorMap tmap_bsf, const PairParams p) {
   static_assert(!A4 || MODE == 0, "the A4W4 path is stage 1 only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
